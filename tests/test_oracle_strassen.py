@@ -1,0 +1,145 @@
+"""Pins for O2, the table-driven Strassen oracle (CPU only)."""
+import itertools
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from oracle import strassen as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.mark.parametrize("levels", [1, 2])
+def test_brent_equations(levels):
+    """sum_p U[p,(i,k)] V[p,(k2,j)] W[(i2,j2),p] = [i=i2][k=k2][j=j2]: the tables compute A.B."""
+    U, V, W = S.tables(levels)
+    g = 2 ** levels
+    assert U.shape == (7 ** levels, g, g) and W.shape == (g, g, 7 ** levels)
+    T = np.einsum("pik,pqj,rsp->ikqjrs", U, V, W)
+    eye = np.eye(g, dtype=np.int64)
+    expect = np.einsum("ir,kq,js->ikqjrs", eye, eye, eye)
+    np.testing.assert_array_equal(T, expect)
+
+
+def test_one_level_tables_have_seven_products_and_18_additions():
+    nnz_u = (S.U1 != 0).sum(axis=1)
+    nnz_v = (S.V1 != 0).sum(axis=1)
+    nnz_w = (S.W1 != 0).sum(axis=1)
+    assert S.U1.shape[0] == 7
+    # operand additions + output additions = 5 + 5 + 8 = 18 (textbook count)
+    assert (nnz_u - 1).sum() + (nnz_v - 1).sum() + (nnz_w - 1).sum() == 18
+
+
+def test_golden_2x2():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "strassen_2x2.txt")):
+        line = line.split("#")[0].split()
+        if line:
+            vals[line[0]] = np.array([float(v) for v in line[1:]])
+    A = vals["A"].reshape(2, 2)
+    B = vals["B"].reshape(2, 2)
+    U, V, W = S.tables(1)
+    At = np.einsum("prc,rc->p", U, A)
+    Bt = np.einsum("prc,rc->p", V, B)
+    np.testing.assert_array_equal(At * Bt, vals["M"])
+    np.testing.assert_array_equal(S.strassen(A, B, 1), vals["C"].reshape(2, 2))
+
+
+def test_brute_force_2x2():
+    """All scalar 2x2 pairs with entries in {-2..2} (5^8 cases) against 8-multiplication products."""
+    r = np.arange(-2, 3)
+    grid = np.array(list(itertools.product(r, repeat=8)), dtype=np.int64)
+    A = grid[:, :4].reshape(-1, 2, 2)
+    B = grid[:, 4:].reshape(-1, 2, 2)
+    U, V, W = S.tables(1)
+    At = np.einsum("prc,nrc->np", U, A)
+    Bt = np.einsum("prc,nrc->np", V, B)
+    C = np.einsum("rcp,np->nrc", W, At * Bt)
+    np.testing.assert_array_equal(C, A @ B)
+
+
+def _recursive_strassen(A, B, levels):
+    """Independent restatement: the 1969 formulas applied recursively (integers)."""
+    if levels == 0:
+        return A @ B
+    m, k = A.shape[0] // 2, A.shape[1] // 2
+    n = B.shape[1] // 2
+    A11, A12, A21, A22 = A[:m, :k], A[:m, k:], A[m:, :k], A[m:, k:]
+    B11, B12, B21, B22 = B[:k, :n], B[:k, n:], B[k:, :n], B[k:, n:]
+    f = lambda x, y: _recursive_strassen(x, y, levels - 1)
+    M1 = f(A11 + A22, B11 + B22)
+    M2 = f(A21 + A22, B11)
+    M3 = f(A11, B12 - B22)
+    M4 = f(A22, B21 - B11)
+    M5 = f(A11 + A12, B22)
+    M6 = f(A21 - A11, B11 + B12)
+    M7 = f(A12 - A22, B21 + B22)
+    return np.block([[M1 + M4 - M5 + M7, M3 + M5], [M2 + M4, M1 - M2 + M3 + M6]])
+
+
+@pytest.mark.parametrize("levels", [1, 2])
+def test_tables_match_recursive_formulas(levels):
+    rng = np.random.default_rng(levels)
+    A = rng.integers(-3, 4, (16, 24)).astype(np.float64)
+    B = rng.integers(-3, 4, (24, 8)).astype(np.float64)
+    np.testing.assert_array_equal(S.strassen(A, B, levels), _recursive_strassen(A, B, levels))
+    np.testing.assert_array_equal(S.strassen(A, B, levels), A @ B)
+
+
+@pytest.mark.parametrize("levels", [1, 2])
+def test_f64_mode_equals_plain_oracle(levels):
+    M, N, K = 64, 96, 128
+    A = synthetic.matrix(M, K, "normal", 21, "bf16")
+    B = synthetic.matrix(N, K, "normal", 22, "bf16")
+    Ab, Bb = synthetic.bits(A), synthetic.bits(B)
+    C1 = oracle.gemm(Ab, Bb, oracle.BF16)
+    C2 = S.strassen(oracle.decode(Ab, 1), oracle.decode(Bb, 1).T, levels, "f64")
+    assert np.linalg.norm(C2 - C1) / np.linalg.norm(C1) < 1e-13
+
+
+@pytest.mark.parametrize("levels", [1, 2])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_emulate_integer_inputs_exact(levels, dtype):
+    """Integer inputs in {-3..3}: every operand sum is exact, so emulation is exact."""
+    dt = oracle.F16 if dtype == "f16" else oracle.BF16
+    M, N, K = 32, 32, 64
+    Ab = synthetic.bits(synthetic.matrix(M, K, "int3", 31, dtype))
+    Bb = synthetic.bits(synthetic.matrix(N, K, "int3", 32, dtype))
+    C2 = S.strassen(oracle.decode(Ab, dt), oracle.decode(Bb, dt).T, levels, "emulate", dt)
+    np.testing.assert_array_equal(C2, oracle.gemm(Ab, Bb, dt))
+
+
+@pytest.mark.parametrize("levels,bound", [(1, 6e-3), (2, 1.2e-2)])
+def test_emulate_error_small_but_nonzero(levels, bound):
+    """BF16 operand-sum rounding adds error of the order of the unit roundoff 2^-9."""
+    M, N, K = 128, 128, 256
+    Ab = synthetic.bits(synthetic.matrix(M, K, "normal", 41, "bf16"))
+    Bb = synthetic.bits(synthetic.matrix(N, K, "normal", 42, "bf16"))
+    C1 = oracle.gemm(Ab, Bb, oracle.BF16)
+    C2 = S.strassen(oracle.decode(Ab, 1), oracle.decode(Bb, 1).T, levels, "emulate", oracle.BF16)
+    err = np.linalg.norm(C2 - C1) / np.linalg.norm(C1)
+    assert 1e-4 < err < bound
+
+
+def test_row_sample_matches_full():
+    M, N, K = 32, 16, 32
+    rng = np.random.default_rng(7)
+    A = rng.standard_normal((M, K))
+    B = rng.standard_normal((K, N))
+    rows = np.array([31, 0, 5, 21, 5])
+    for levels in (1, 2):
+        for mode in ("f64", "emulate"):
+            full = S.strassen(A, B, levels, mode, oracle.BF16)
+            np.testing.assert_array_equal(S.strassen(A, B, levels, mode, oracle.BF16, rows=rows), full[rows])
+
+
+def test_planted_sign_error_is_caught():
+    """A single flipped sign in W (e.g. C22 = M1 + M2 + ...) breaks the Brent equations."""
+    Wbad = S.W1.copy()
+    Wbad[3, 1] = 1
+    T = np.einsum("pik,pqj,rsp->ikqjrs", S.U1.reshape(7, 2, 2), S.V1.reshape(7, 2, 2), Wbad.reshape(2, 2, 7))
+    eye = np.eye(2, dtype=np.int64)
+    assert not np.array_equal(T, np.einsum("ir,kq,js->ikqjrs", eye, eye, eye))
