@@ -1,0 +1,364 @@
+// C ABI of lcgemm: handle, argument checks, tensor-map encoding, algorithm
+// dispatch and the host-buffer entry point.  See include/lcgemm.h for the
+// contract of every entry point.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "lcgemm.h"
+#include "runtime.h"
+
+using namespace lcg;
+
+namespace lcg {
+
+// ---------------------------------------------------------------- tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5];
+  cuuint64_t s[4];
+  cuuint32_t b[5];
+  cuuint32_t e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// K-major 2-D operand: `rows` rows of `k` contiguous elements, `ld` apart,
+// read in boxes of 64 (K) x box_rows.
+bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, int64_t k, int64_t ld,
+                   int box_rows) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(ld) * 2};
+  const uint32_t box[2] = {64u, static_cast<uint32_t>(box_rows)};
+  return encode_map(m, bf16, base, 2, dims, strides, box);
+}
+
+}  // namespace lcg
+
+// ---------------------------------------------------------------- helpers
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+int check_shape(int64_t M, int64_t N, int64_t K, int dtype, int algo) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return LCGEMM_ERR_ARG;
+  if (dtype != LCGEMM_F16 && dtype != LCGEMM_BF16) return LCGEMM_ERR_ARG;
+  if (algo < LCGEMM_PLAIN || algo > LCGEMM_STRASSEN1_UNFUSED) return LCGEMM_ERR_ARG;
+  return LCGEMM_OK;
+}
+
+int check_device_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      const void* C, int64_t ldc) {
+  if (!C || ldc < N) return LCGEMM_ERR_ARG;
+  if (K > 0 && (!A || !B || lda < K || ldb < K)) return LCGEMM_ERR_ARG;
+  if (ldc > (int64_t(1) << 36) || lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36)) return LCGEMM_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 15u) || (ldc & 7)) return LCGEMM_ERR_ALIGN;
+  if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+                (lda & 7) || (ldb & 7)))
+    return LCGEMM_ERR_ALIGN;
+  const int64_t c_bytes = ((M - 1) * ldc + N) * 2;
+  if (K > 0) {
+    if (overlaps(C, c_bytes, A, ((M - 1) * lda + K) * 2)) return LCGEMM_ERR_ALIAS;
+    if (overlaps(C, c_bytes, B, ((N - 1) * ldb + K) * 2)) return LCGEMM_ERR_ALIAS;
+  }
+  return LCGEMM_OK;
+}
+
+int take_error(lcgemm_ctx* h) {
+  volatile int* e = h->err_host;
+  const int v = *e;
+  if (v) *e = 0;
+  return v ? LCGEMM_ERR_TIMEOUT : LCGEMM_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- plain path
+
+namespace lcg {
+
+int grid_cap(const lcgemm_ctx* h) {
+  return h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms;
+}
+
+int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+              int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
+  PlainLaunch L{};
+  L.bf16 = bf16;
+  L.bn = N <= 128 ? 128 : 256;
+  if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, kPlainBM)) return LCGEMM_ERR_CUDA;
+  if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, L.bn)) return LCGEMM_ERR_CUDA;
+  PlainArgs& a = L.args;
+  a.C = C;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.tiles_m = static_cast<int>((M + kPlainBM - 1) / kPlainBM);
+  a.tiles_n = static_cast<int>((N + L.bn - 1) / L.bn);
+  const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n;
+  if (tiles > kMaxDim) return LCGEMM_ERR_UNSUPPORTED;
+  a.num_tiles = static_cast<int>(tiles);
+  a.group_m = 16;
+  a.err = h->err_dev;
+  a.timeout_ns = h->timeout_ns;
+  L.grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap(h)));
+  return launch_plain(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+}
+
+}  // namespace lcg
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+int lcgemm_create(lcgemm_t* out, int device) {
+  if (!out) return LCGEMM_ERR_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) return LCGEMM_ERR_ARG;
+  DeviceGuard g(device);
+  if (!g.ok) return LCGEMM_ERR_CUDA;
+  auto* h = new (std::nothrow) lcgemm_ctx();
+  if (!h) return LCGEMM_ERR_NOMEM;
+  h->device = device;
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete h;
+    return LCGEMM_ERR_CUDA;
+  }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), 64, cudaHostAllocMapped) != cudaSuccess) {
+    delete h;
+    return LCGEMM_ERR_NOMEM;
+  }
+  *h->err_host = 0;
+  if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err_dev), h->err_host, 0) != cudaSuccess) {
+    cudaFreeHost(h->err_host);
+    delete h;
+    return LCGEMM_ERR_CUDA;
+  }
+  if (const char* s = std::getenv("LCGEMM_PEAK_GFLOPS")) {
+    const double v = std::atof(s);
+    if (v > 0) h->peak_gflops = v;
+  }
+  if (const char* s = std::getenv("LCGEMM_HBM_GBPS")) {
+    const double v = std::atof(s);
+    if (v > 0) h->hbm_gbps = v;
+  }
+  *out = h;
+  return LCGEMM_OK;
+}
+
+int lcgemm_destroy(lcgemm_t h) {
+  if (!h) return LCGEMM_OK;
+  DeviceGuard g(h->device);
+  cudaDeviceSynchronize();
+  if (h->ws) cudaFree(h->ws);
+  if (h->stage) cudaFree(h->stage);
+  if (h->err_host) cudaFreeHost(h->err_host);
+  delete h;
+  return LCGEMM_OK;
+}
+
+int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+               void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
+  if (!h) return LCGEMM_ERR_ARG;
+  int rc = check_shape(M, N, K, dtype, algo);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return LCGEMM_OK;
+  rc = check_device_args(M, N, K, A, lda, B, ldb, C, ldc);
+  if (rc) return rc;
+  rc = take_error(h);
+  if (rc) return rc;
+  DeviceGuard g(h->device);
+  if (!g.ok) return LCGEMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (K == 0) {
+    if (cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(N) * 2, static_cast<size_t>(M),
+                          st) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+    h->last_algo = LCGEMM_PLAIN;
+    return LCGEMM_OK;
+  }
+  const bool bf16 = dtype == LCGEMM_BF16;
+  int chosen = algo == LCGEMM_AUTO ? select_algo(h, M, N, K, dtype) : algo;
+  rc = dispatch(h, chosen, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+  if (rc == LCGEMM_OK) h->last_algo = chosen;
+  return rc;
+}
+
+int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
+  if (!h) return LCGEMM_ERR_ARG;
+  int rc = check_shape(M, N, K, dtype, algo);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return LCGEMM_OK;
+  if (!C || ldc < N || (K > 0 && (!A || !B || lda < K || ldb < K))) return LCGEMM_ERR_ARG;
+  DeviceGuard g(h->device);
+  if (!g.ok) return LCGEMM_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // device staging: pitches rounded up to 8 elements (16 bytes), 256-byte aligned sub-buffers
+  const int64_t kp = std::max<int64_t>(8, (K + 7) / 8 * 8);
+  const int64_t np = (N + 7) / 8 * 8;
+  auto rup = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t a_bytes = rup(M * kp * 2), b_bytes = rup(N * kp * 2), c_bytes = rup(M * np * 2);
+  const size_t need = static_cast<size_t>(a_bytes + b_bytes + c_bytes);
+  if (need > h->stage_bytes) {
+    if (h->stage) {
+      cudaStreamSynchronize(st);
+      cudaFree(h->stage);
+      h->stage = nullptr;
+      h->stage_bytes = 0;
+    }
+    if (cudaMalloc(&h->stage, need) != cudaSuccess) {
+      h->stage = nullptr;
+      return LCGEMM_ERR_NOMEM;
+    }
+    h->stage_bytes = need;
+  }
+  char* dA = static_cast<char*>(h->stage);
+  char* dB = dA + a_bytes;
+  char* dC = dB + b_bytes;
+  if (K > 0) {
+    if (cudaMemcpy2DAsync(dA, kp * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpy2DAsync(dB, kp * 2, B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+  }
+  rc = lcgemm_run(h, M, N, K, dA, kp, dB, kp, dC, np, dtype, algo, cuda_stream);
+  if (rc) return rc;
+  if (cudaMemcpy2DAsync(C, ldc * 2, dC, np * 2, N * 2, M, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return LCGEMM_ERR_CUDA;
+  return LCGEMM_OK;
+}
+
+int lcgemm_last_algo(lcgemm_t h) { return h ? h->last_algo : LCGEMM_ERR_ARG; }
+
+int lcgemm_select(lcgemm_t h, int64_t M, int64_t N, int64_t K, int dtype) {
+  if (!h) return LCGEMM_ERR_ARG;
+  const int rc = check_shape(M, N, K, dtype, LCGEMM_AUTO);
+  if (rc) return rc;
+  return select_algo(h, M, N, K, dtype);
+}
+
+int lcgemm_estimate(lcgemm_t h, int64_t M, int64_t N, int64_t K, int dtype, int algo, double* seconds) {
+  if (!h || !seconds) return LCGEMM_ERR_ARG;
+  int rc = check_shape(M, N, K, dtype, algo);
+  if (rc) return rc;
+  if (algo == LCGEMM_AUTO) algo = select_algo(h, M, N, K, dtype);
+  if (!algo_supported(algo, M, N, K)) return LCGEMM_ERR_UNSUPPORTED;
+  *seconds = estimate_seconds(h, algo, M, N, K);
+  return LCGEMM_OK;
+}
+
+int lcgemm_sync_status(lcgemm_t h, void* cuda_stream) {
+  if (!h) return LCGEMM_ERR_ARG;
+  DeviceGuard g(h->device);
+  if (!g.ok) return LCGEMM_ERR_CUDA;
+  const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  const int rc = take_error(h);
+  if (rc) return rc;
+  return e == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+}
+
+int lcgemm_set_option(lcgemm_t h, int option, int64_t value) {
+  if (!h) return LCGEMM_ERR_ARG;
+  switch (option) {
+    case LCGEMM_OPT_WAIT_TIMEOUT_US:
+      if (value <= 0 || value > int64_t(60) * 1000000) return LCGEMM_ERR_ARG;
+      h->timeout_ns = static_cast<uint64_t>(value) * 1000u;
+      return LCGEMM_OK;
+    case LCGEMM_OPT_GROUP_ORDER:
+      if (value != 0 && value != 1) return LCGEMM_ERR_ARG;
+      h->group_order = static_cast<int>(value);
+      return LCGEMM_OK;
+    case LCGEMM_OPT_SPLIT:
+      if (value != 0 && value != 1) return LCGEMM_ERR_ARG;
+      h->split = static_cast<int>(value);
+      return LCGEMM_OK;
+    case LCGEMM_OPT_MAX_CTAS:
+      if (value < 0 || value > 65536) return LCGEMM_ERR_ARG;
+      h->max_ctas = static_cast<int>(value);
+      return LCGEMM_OK;
+    case LCGEMM_OPT_PEAK_GFLOPS:
+      if (value <= 0) return LCGEMM_ERR_ARG;
+      h->peak_gflops = static_cast<double>(value);
+      return LCGEMM_OK;
+    case LCGEMM_OPT_HBM_GBPS:
+      if (value <= 0) return LCGEMM_ERR_ARG;
+      h->hbm_gbps = static_cast<double>(value);
+      return LCGEMM_OK;
+    case LCGEMM_OPT_DEBUG_DROP_SIGNAL:
+      if (value != 0 && value != 1) return LCGEMM_ERR_ARG;
+      h->debug_drop = static_cast<int>(value);
+      return LCGEMM_OK;
+    default:
+      return LCGEMM_ERR_ARG;
+  }
+}
+
+const char* lcgemm_strerror(int code) {
+  switch (code) {
+    case LCGEMM_OK: return "ok";
+    case LCGEMM_ERR_ARG: return "invalid argument";
+    case LCGEMM_ERR_ALIGN: return "pointer not 16-byte aligned or leading dimension not a multiple of 8";
+    case LCGEMM_ERR_UNSUPPORTED: return "algorithm does not support these dimensions";
+    case LCGEMM_ERR_ALIAS: return "C overlaps A or B";
+    case LCGEMM_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case LCGEMM_ERR_TIMEOUT: return "a bounded device-side wait gave up in an earlier launch";
+    case LCGEMM_ERR_NOMEM: return "workspace allocation failed";
+    default: return "unknown status code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,246 @@
+// Persistent plain GEMM for sm_103a: C = A . B, FP16/BF16 in, FP32 accumulate
+// in tensor memory, one round-to-nearest-even cast on the way out.
+//
+// One CTA per SM walks a grouped raster of 128 x BN output tiles.  Warp roles:
+//   warp 0      TMA producer: A (128 x 64) and B (BN x 64) K-slabs into a
+//               STAGES-deep shared-memory ring (full/empty mbarriers)
+//   warp 1      TMEM allocator and MMA issuer: 4 tcgen05.mma (K = 16 each)
+//               per slab into one of two TMEM accumulators
+//   warps 2..5  epilogue: tcgen05.ld -> cvt.rn -> global stores, overlapped
+//               with the next tile's main loop through the second accumulator
+//
+// Prior art for the tiling, the multi-stage prefetch and the block swizzle:
+// CUDA-L2 summary (gist.science 2512.02551), "discovered techniques" list
+// (double-buffering, multi-step prefetch, block swizzling for L2 hit rate).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lcg {
+
+namespace {
+
+constexpr int kBM = kPlainBM;
+constexpr int kBK = kPlainBK;
+constexpr int kThreads = 192;
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& mb, int& nb) {
+  const int group_tiles = a.group_m * a.tiles_n;
+  const int g = tile / group_tiles;
+  const int first_m = g * a.group_m;
+  const int rows = min(a.tiles_m - first_m, a.group_m);
+  const int local = tile - g * group_tiles;
+  mb = first_m + local % rows;
+  nb = local / rows;
+}
+
+template <int BN, int STAGES, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    plain_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const PlainArgs args) {
+  using C = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * C::kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
+  const int num_kb = (args.K + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, args, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBK, mb * kBM);
+          tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, nb * BN);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // The CTA is aborting: let every copy this thread started land first.
+        for (int s = 0; s < STAGES; ++s)
+          if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, wc, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(BF16, kBM, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_f16(d_tmem, sdesc_k128(a0 + k * 32), sdesc_k128(b0 + k * 32), idesc, (kb | k) != 0);
+          mma_commit(&empty[stage]);
+          issued = true;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok && issued) {
+        // Aborting: the tensor core must be done with TMEM before it is freed.
+        mma_commit(drain);
+        mbar_wait(drain, 0, wc, false);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t acc = 0, acc_phase = 0;
+    uint16_t* Cp = static_cast<uint16_t*>(args.C);
+    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, args, mb, nb);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const int row = mb * kBM + q * 32 + lane;
+      uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c * 32, r);
+        tmem_wait_ld();
+        const int col = nb * BN + c * 32;
+        if (row < args.M && col < args.N) {
+          if (col + 32 <= args.N) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
+              o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
+              o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
+              o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
+              dst[v] = o;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
+              if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
+              if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, bool BF16>
+cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
+  using C = Cfg<BN, STAGES>;
+  auto kern = plain_gemm_kernel<BN, STAGES, BF16>;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tmA, L.tmB, L.args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream) {
+  if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true>(L, stream) : launch_impl<256, 4, false>(L, stream);
+  if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true>(L, stream) : launch_impl<128, 6, false>(L, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lcg

@@ -1,0 +1,45 @@
+// Host runtime shared by the C ABI, the dispatcher and the cost model.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+struct lcgemm_ctx {
+  int device = 0;
+  int num_sms = 0;
+  int* err_host = nullptr;   // mapped, page-locked error word (host view)
+  int* err_dev = nullptr;    // the same word as the device sees it
+  uint64_t timeout_ns = 2000000000ull;
+  int group_order = 1;
+  int split = 1;
+  int max_ctas = 0;
+  int debug_drop = 0;
+  double peak_gflops = 2.25e6;  // dense FP16/BF16 tensor peak (GFLOP/s)
+  double hbm_gbps = 8000.0;     // HBM bandwidth (GB/s)
+  int last_algo = -1;
+  void* ws = nullptr;           // Strassen workspace (summed operands, partials, flags)
+  size_t ws_bytes = 0;
+  void* stage = nullptr;        // staging for lcgemm_run_host
+  size_t stage_bytes = 0;
+};
+
+namespace lcg {
+
+bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box);
+bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows);
+int grid_cap(const lcgemm_ctx* h);
+
+int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+              int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st);
+
+// Dispatcher and cost model (runtime.cu).
+bool algo_supported(int algo, int64_t M, int64_t N, int64_t K);
+int select_algo(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, int dtype);
+double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K);
+int dispatch(lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+             int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st);
+
+}  // namespace lcg

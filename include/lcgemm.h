@@ -1,0 +1,158 @@
+/*
+ * lcgemm -- half-precision GEMM for GB300 (sm_103a): plain tiled GEMM and the
+ * low-complexity (LCMA / Strassen) path, behind a plain C ABI.
+ *
+ * Operation (every entry point): C = A . B with FP16 or BF16 inputs, FP32
+ * accumulation and one round-to-nearest-even cast to the input type.
+ *   - plain:     one persistent tensor-core kernel.
+ *   - strassen1: one-level Strassen -- 7 block products instead of 8, the A and
+ *                B sub-blocks combined before the products and the products
+ *                recombined into the four quadrants of C (FalconGEMM write-up,
+ *                hyper.ai news 54396, section "从 Strassen 出发"; the
+ *                combine / product / recombine pipeline and its fusion are in
+ *                section "从 LCMA 到 FalconGEMM").
+ *   - strassen2: two-level Strassen, 49 block products over a 4x4 block grid
+ *                (same section: 49 instead of 64 block multiplications).
+ *   - auto:      a roofline-style cost model picks one of the above per shape
+ *                (section "从缓存重排到 Cost Model").
+ * The one-level scheme is the textbook Strassen (1969) formulas:
+ *   M1=(A11+A22)(B11+B22) M2=(A21+A22)B11 M3=A11(B12-B22) M4=A22(B21-B11)
+ *   M5=(A11+A12)B22 M6=(A21-A11)(B11+B12) M7=(A12-A22)(B21+B22)
+ *   C11=M1+M4-M5+M7 C12=M3+M5 C21=M2+M4 C22=M1-M2+M3+M6
+ *
+ * Layouts (element type = dtype for A, B and C):
+ *   A : row-major M x K, element (i,k) at A[i*lda + k], lda >= K
+ *   B : the K x N operand stored column-major, element (k,j) at B[j*ldb + k],
+ *       ldb >= K (both operands are K-contiguous)
+ *   C : row-major M x N, element (i,j) at C[i*ldc + j], ldc >= N
+ *
+ * Alignment (the tensor-memory-access engine reads A and B): A, B and C must
+ * be 16-byte aligned and lda, ldb, ldc multiples of 8 elements.  There is no
+ * fallback path: misaligned calls fail with LCGEMM_ERR_ALIGN.
+ *
+ * Errors: every entry point returns an int, 0 = LCGEMM_OK, negative on
+ * failure; nothing is thrown across the ABI.  Argument checks happen on the
+ * host before anything is launched.  Device-side waits are bounded; a wait
+ * that gives up records LCGEMM_ERR_TIMEOUT, which the NEXT lcgemm_run on the
+ * handle or lcgemm_sync_status returns (and clears).
+ *
+ * Numerics: NaN and Inf propagate per IEEE with no checks on the hot path.
+ * In the Strassen paths an Inf in one block can turn into NaN in other
+ * blocks (Inf - Inf in the operand sums or the recombination).
+ *
+ * Threading: a handle may be used by one host thread at a time, and runs
+ * through one handle must not overlap on different streams (they share the
+ * handle's workspace).
+ */
+#ifndef LCGEMM_H
+#define LCGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LCGEMM_API __attribute__((visibility("default")))
+#else
+#define LCGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lcgemm_ctx* lcgemm_t;
+
+/* element type of A, B and C */
+enum { LCGEMM_F16 = 0, LCGEMM_BF16 = 1 };
+
+/* algorithm */
+enum {
+  LCGEMM_PLAIN = 0,             /* persistent tiled GEMM                                  */
+  LCGEMM_STRASSEN1 = 1,         /* one-level Strassen: combine pre-pass + fused products  */
+  LCGEMM_STRASSEN2 = 2,         /* two-level Strassen (49 products)                       */
+  LCGEMM_AUTO = 3,              /* cost model chooses among the three above               */
+  LCGEMM_STRASSEN1_UNFUSED = 4  /* ablation: combine, 7 products written to HBM in FP32,
+                                   separate recombination kernel (the basic pipeline)     */
+};
+
+/* status codes */
+enum {
+  LCGEMM_OK = 0,
+  LCGEMM_ERR_ARG = -1,          /* null pointer, negative size, ld too small, bad enum    */
+  LCGEMM_ERR_ALIGN = -2,        /* pointer not 16-byte aligned or ld not a multiple of 8  */
+  LCGEMM_ERR_UNSUPPORTED = -3,  /* explicit Strassen on dimensions it cannot split        */
+  LCGEMM_ERR_ALIAS = -4,        /* C overlaps A or B                                      */
+  LCGEMM_ERR_CUDA = -5,         /* a CUDA runtime/driver call or launch failed            */
+  LCGEMM_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up (earlier launch)    */
+  LCGEMM_ERR_NOMEM = -7         /* workspace or staging allocation failed                 */
+};
+
+/* options for lcgemm_set_option */
+enum {
+  LCGEMM_OPT_WAIT_TIMEOUT_US = 1,  /* bound on every device-side wait, microseconds (default 2000000) */
+  LCGEMM_OPT_GROUP_ORDER = 2,      /* 1: order Strassen waves by product type (default), 0: off       */
+  LCGEMM_OPT_SPLIT = 3,            /* 1: split tail Groups across two CTAs (default), 0: off          */
+  LCGEMM_OPT_MAX_CTAS = 4,         /* cap on the persistent grid (default 0 = one CTA per SM)         */
+  LCGEMM_OPT_PEAK_GFLOPS = 5,      /* cost model: dense FP16/BF16 tensor peak, GFLOP/s                */
+  LCGEMM_OPT_HBM_GBPS = 6,         /* cost model: HBM bandwidth, GB/s                                 */
+  LCGEMM_OPT_DEBUG_DROP_SIGNAL = 7 /* test hook: a split Group's partner never signals, so the
+                                      owner's bounded wait runs out (no fault, no hang)               */
+};
+
+/*
+ * Create a handle bound to CUDA device `device`.  Allocates only a few bytes
+ * (the mapped error word); the Strassen workspace grows on first use.
+ * Reads environment overrides LCGEMM_PEAK_GFLOPS and LCGEMM_HBM_GBPS.
+ * Returns LCGEMM_ERR_ARG for a null `out` or an invalid device.
+ */
+LCGEMM_API int lcgemm_create(lcgemm_t* out, int device);
+
+/* Synchronise the device, free the workspace and the handle.  Null is a no-op. */
+LCGEMM_API int lcgemm_destroy(lcgemm_t h);
+
+/*
+ * C = A . B, asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy
+ * default stream).  A, B, C are device pointers owned by the caller; C is
+ * overwritten (beta = 0).  M = 0 or N = 0 is a no-op; K = 0 writes zeros.
+ * LCGEMM_AUTO never fails with LCGEMM_ERR_UNSUPPORTED: it falls back to plain.
+ * Explicit LCGEMM_STRASSEN1 needs M, N even and K a multiple of 16;
+ * LCGEMM_STRASSEN2 needs M, N multiples of 4 and K a multiple of 32.
+ */
+LCGEMM_API int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda, const void* B, int64_t ldb,
+               void* C, int64_t ldc, int dtype, int algo, void* cuda_stream);
+
+/*
+ * Same operation on HOST buffers (same layouts): copies A and B to device
+ * staging buffers owned by the handle, runs lcgemm_run, copies C back, all
+ * enqueued on `cuda_stream`.  The call returns once the work is enqueued;
+ * synchronise the stream before reading C.  Page-locked host memory gives
+ * asynchronous copies; pageable memory works but the copies block.
+ */
+LCGEMM_API int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K,
+                    const void* A, int64_t lda, const void* B, int64_t ldb,
+                    void* C, int64_t ldc, int dtype, int algo, void* cuda_stream);
+
+/* Algorithm the last successful lcgemm_run on this handle executed (LCGEMM_PLAIN..). */
+LCGEMM_API int lcgemm_last_algo(lcgemm_t h);
+
+/* Algorithm LCGEMM_AUTO would execute for this shape (>= 0), or a negative status. */
+LCGEMM_API int lcgemm_select(lcgemm_t h, int64_t M, int64_t N, int64_t K, int dtype);
+
+/* Cost-model time estimate in seconds for `algo` on this shape (no launch). */
+LCGEMM_API int lcgemm_estimate(lcgemm_t h, int64_t M, int64_t N, int64_t K, int dtype, int algo,
+                    double* seconds);
+
+/* Synchronise `cuda_stream`, then return and clear the device error word. */
+LCGEMM_API int lcgemm_sync_status(lcgemm_t h, void* cuda_stream);
+
+/* Set an LCGEMM_OPT_* option.  Returns LCGEMM_ERR_ARG for unknown keys or bad values. */
+LCGEMM_API int lcgemm_set_option(lcgemm_t h, int option, int64_t value);
+
+/* Static description of a status code (never NULL). */
+LCGEMM_API const char* lcgemm_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCGEMM_H */

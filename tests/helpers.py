@@ -1,0 +1,64 @@
+"""Shared helpers for the parity tests: run the library, run the oracle, compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synthetic
+
+# Floating-point tolerances on N(0,1)-type inputs, normwise relative Frobenius
+# error against the unrounded FP64 product, per algorithm family and dtype.
+NORMWISE_TOL = {
+    ("plain", "f16"): 2e-3,
+    ("plain", "bf16"): 8e-3,
+    ("strassen", "f16"): 4e-3,
+    ("strassen", "bf16"): 1.6e-2,
+}
+# max_ij |C_gpu - C64| <= MAXERR_SIGMA * sigma_C, sigma_C = RMS(C64)
+MAXERR_SIGMA = 0.05
+
+
+def family(algo: str) -> str:
+    return "plain" if algo == "plain" else "strassen"
+
+
+def dt_code(dtype: str) -> int:
+    return oracle.F16 if dtype == "f16" else oracle.BF16
+
+
+def oracle_c64(A: torch.Tensor, B: torch.Tensor, dtype: str, rows=None) -> np.ndarray:
+    return oracle.gemm(synthetic.bits(A), synthetic.bits(B), dt_code(dtype), rows=rows)
+
+
+def gpu_values(C: torch.Tensor, rows=None) -> np.ndarray:
+    Ch = C.detach().cpu()
+    if rows is not None:
+        Ch = Ch[torch.as_tensor(rows)]
+    return Ch.to(torch.float64).numpy()
+
+
+def assert_bit_exact(C: torch.Tensor, C64: np.ndarray, dtype: str, rows=None):
+    ref = oracle.reference_output(C64, dt_code(dtype))
+    got = synthetic.bits(C if rows is None else C.detach().cpu()[torch.as_tensor(rows)])
+    bad = np.nonzero(got != ref)
+    assert bad[0].size == 0, f"{bad[0].size} mismatches, first at {bad[0][0]},{bad[1][0]}: " \
+                             f"got {got[bad][0]:#06x} want {ref[bad][0]:#06x}"
+
+
+def errors(C: torch.Tensor, C64: np.ndarray, rows=None):
+    got = gpu_values(C, rows)
+    diff = got - C64
+    nrm = np.linalg.norm(C64)
+    normwise = np.linalg.norm(diff) / nrm if nrm > 0 else np.linalg.norm(diff)
+    sigma = np.sqrt(np.mean(C64 ** 2))
+    return normwise, float(np.max(np.abs(diff))) if diff.size else 0.0, sigma
+
+
+def assert_close(C: torch.Tensor, C64: np.ndarray, dtype: str, algo: str, rows=None):
+    assert np.isfinite(gpu_values(C, rows)).all(), "non-finite output"
+    normwise, maxerr, sigma = errors(C, C64, rows)
+    tol = NORMWISE_TOL[(family(algo), dtype)]
+    assert normwise <= tol, f"normwise error {normwise:.3e} > {tol:.1e} ({algo}, {dtype})"
+    assert maxerr <= MAXERR_SIGMA * sigma, f"max error {maxerr:.3e} > {MAXERR_SIGMA} * sigma_C ({sigma:.3e})"
+    return normwise, maxerr, sigma

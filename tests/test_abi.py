@@ -1,0 +1,68 @@
+"""The C-ABI library loads and exports every entry point include/lcgemm.h declares (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import complexity_matmul_gb300 as lcg
+from complexity_matmul_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"LCGEMM_API\s+[\w\s\*]*?\b(lcgemm_\w+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def library():
+    _build.build()
+    return lcg.lib()
+
+
+def test_library_exports_all_declared_symbols(library):
+    declared = _declared()
+    assert {"lcgemm_create", "lcgemm_run", "lcgemm_destroy"} <= declared
+    missing = [n for n in sorted(declared) if not hasattr(library, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert set(lcg.EXPORTS) <= declared
+
+
+def test_strerror_is_static_and_total(library):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 12345):
+        s = library.lcgemm_strerror(code)
+        assert isinstance(s, bytes) and s
+    assert b"aligned" in library.lcgemm_strerror(-2)
+
+
+def test_null_handle_rejected_without_gpu(library):
+    assert library.lcgemm_run(None, 8, 8, 8, None, 8, None, 8, None, 8, 1, 0, None) == lcg.ERR_ARG
+    assert library.lcgemm_set_option(None, 1, 5) == lcg.ERR_ARG
+    assert library.lcgemm_last_algo(None) == lcg.ERR_ARG
+    assert library.lcgemm_destroy(None) == lcg.OK
+    assert library.lcgemm_create(None, 0) == lcg.ERR_ARG
+
+
+def test_create_fails_cleanly_without_device(library):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    assert library.lcgemm_create(ctypes.byref(h), 0) == lcg.ERR_ARG
+    assert not h.value
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The package never imports, links or executes anything under oracle/."""
+    pkg = os.path.join(ROOT, "complexity_matmul_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in text.lower(), fn

@@ -1,0 +1,171 @@
+"""Parity of the plain persistent GEMM against the CPU oracle (GPU, through the C ABI)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import complexity_matmul_gb300 as lcg
+import synthetic
+from helpers import assert_bit_exact, assert_close, oracle_c64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    handle = lcg.Handle(0)
+    yield handle
+    handle.close()
+
+
+def _run(h, A, B, algo="plain"):
+    C = h.run(A, B, algo=algo)
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    return C
+
+
+# ---------------------------------------------------------------- 256^3 FP16 (small square workload)
+
+@pytest.mark.parametrize("dist", ["int3", "binary"])
+def test_small_square_integer_bit_exact(h, dist):
+    A, B = synthetic.operands(256, 256, 256, dist, 1, "f16", "cuda")
+    assert_bit_exact(_run(h, A, B), oracle_c64(A, B, "f16"), "f16")
+
+
+def test_small_square_uniform(h):
+    A, B = synthetic.operands(256, 256, 256, "uniform", 1, "f16", "cuda")
+    C = _run(h, A, B)
+    C64 = oracle_c64(A, B, "f16")
+    assert_close(C, C64, "f16", "plain")
+    # FP32 accumulation sits far below one FP16 ulp: nearly every element is the correctly rounded value
+    ref = torch.from_numpy(C64).to(torch.float16)
+    assert (C.cpu() == ref).float().mean().item() > 0.98
+
+
+# ---------------------------------------------------------------- ragged shapes (tiles, tails, K tails)
+
+RAGGED = [(1, 128, 4096), (1, 8, 8), (7, 9, 24), (129, 257, 72), (200, 300, 136), (128, 256, 64),
+          (300, 130, 1000), (513, 384, 520), (64, 1024, 16), (1000, 24, 8)]
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_ragged_integer_bit_exact(h, M, N, K, dtype):
+    # integer inputs, K <= 4096: |C| <= 9K < 2^24 so FP32 accumulation is exact; one rounding either side
+    A, B = synthetic.operands(M, N, K, "int3", 7, dtype, "cuda")
+    assert_bit_exact(_run(h, A, B), oracle_c64(A, B, dtype), dtype)
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 257, 72), (513, 384, 520), (300, 130, 1000)])
+def test_ragged_normal(h, M, N, K):
+    A, B = synthetic.operands(M, N, K, "normal", 8, "bf16", "cuda")
+    assert_close(_run(h, A, B), oracle_c64(A, B, "bf16"), "bf16", "plain")
+
+
+def test_strided_operands(h):
+    """Leading dimensions larger than the row length (sub-matrix views)."""
+    M, N, K = 192, 320, 200
+    Abig = synthetic.matrix(M, 264, "int3", 9, "bf16", "cuda")
+    Bbig = synthetic.matrix(N, 216, "int3", 10, "bf16", "cuda")
+    Cbig = torch.full((M, 400), 7.0, dtype=torch.bfloat16, device="cuda")
+    A, B, C = Abig[:, :K], Bbig[:, :K], Cbig[:, 16:16 + N]
+    h.run(A, B, C)
+    torch.cuda.synchronize()
+    assert_bit_exact(C, oracle_c64(A.contiguous(), B.contiguous(), "bf16"), "bf16")
+    # nothing outside the C view was written
+    assert (Cbig[:, :16] == 7).all() and (Cbig[:, 16 + N:] == 7).all()
+
+
+# ---------------------------------------------------------------- square sweep (BF16 N(0,1))
+
+def test_square_2048_full(h):
+    A, B = synthetic.operands(2048, 2048, 2048, "normal", 2, "bf16", "cuda")
+    assert_close(_run(h, A, B), oracle_c64(A, B, "bf16"), "bf16", "plain")
+
+
+@pytest.mark.parametrize("n", [4096, 8192, 16384])
+def test_square_sampled_rows(h, n):
+    A, B = synthetic.operands(n, n, n, "normal", 2, "bf16", "cuda")
+    C = _run(h, A, B)
+    rows = synthetic.row_sample(n, 64 if n == 16384 else 128)
+    assert_close(C, oracle_c64(A, B, "bf16", rows=rows), "bf16", "plain", rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 14336, 4096), (16, 4096, 14336), (128, 14336, 4096), (1024, 4096, 14336)])
+def test_llm_skinny(h, M, N, K):
+    A = synthetic.matrix(M, K, "normal", 1004, "bf16", "cuda")
+    B = synthetic.matrix(N, K, "normal", 2004, "bf16", "cuda", scale=0.02)
+    C = _run(h, A, B)
+    rows = synthetic.row_sample(M, 32)
+    assert_close(C, oracle_c64(A, B, "bf16", rows=rows), "bf16", "plain", rows=rows)
+
+
+# ---------------------------------------------------------------- identities and edge cases
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_identity_bit_exact(h, dtype):
+    n = 384
+    A = synthetic.matrix(n, n, "normal", 12, dtype, "cuda")
+    eye = torch.eye(n, dtype=A.dtype, device="cuda")
+    assert torch.equal(_run(h, A, eye), A)
+
+
+def test_linearity(h):
+    """(A1 + A2).B = A1.B + A2.B exactly: FP16 integers with |C| <= 6*3*64 < 2048 are all representable."""
+    M, N, K = 256, 512, 64
+    A1 = synthetic.matrix(M, K, "int3", 13, "f16", "cuda")
+    A2 = synthetic.matrix(M, K, "int3", 14, "f16", "cuda")
+    B = synthetic.matrix(N, K, "int3", 15, "f16", "cuda")
+    lhs = _run(h, (A1.float() + A2.float()).to(torch.float16), B).float()
+    rhs = _run(h, A1, B).float() + _run(h, A2, B).float()
+    assert torch.equal(lhs, rhs)
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop(h):
+    A = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((32, 0), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((64, 32), 3.0, dtype=torch.bfloat16, device="cuda")
+    rc = h.run_raw(64, 32, 0, A.data_ptr(), 8, B.data_ptr(), 8, C.data_ptr(), 32, lcg.BF16, lcg.PLAIN,
+                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == 0 and (C == 0).all()
+    C.fill_(5.0)
+    assert h.run_raw(0, 32, 16, None, 16, None, 16, C.data_ptr(), 32, lcg.BF16, lcg.PLAIN, None) == 0
+    assert h.run_raw(64, 0, 16, None, 16, None, 16, C.data_ptr(), 32, lcg.BF16, lcg.PLAIN, None) == 0
+    torch.cuda.synchronize()
+    assert (C == 5).all()
+
+
+def test_repeated_launches_stable(h):
+    """Many back-to-back launches (mbarrier phase logic across CTAs' tile loops) stay exact."""
+    A, B = synthetic.operands(1024, 1536, 704, "int3", 16, "f16", "cuda")
+    ref = oracle_c64(A, B, "f16")
+    Cs = [h.run(A, B) for _ in range(20)]
+    torch.cuda.synchronize()
+    for C in Cs[::5]:
+        assert_bit_exact(C, ref, "f16")
+    assert all(torch.equal(Cs[0], C) for C in Cs)
+
+
+# ---------------------------------------------------------------- argument errors (host-side only)
+
+def test_argument_errors(h):
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    a, b, c = A.data_ptr(), B.data_ptr(), C.data_ptr()
+    run = h.run_raw
+    assert run(-1, 64, 64, a, 64, b, 64, c, 64, 1, 0) == lcg.ERR_ARG
+    assert run(64, 64, 64, a, 63, b, 64, c, 64, 1, 0) == lcg.ERR_ARG          # lda < K
+    assert run(64, 64, 64, a, 64, b, 64, c, 60, 1, 0) == lcg.ERR_ARG          # ldc < N
+    assert run(64, 64, 64, None, 64, b, 64, c, 64, 1, 0) == lcg.ERR_ARG
+    assert run(64, 64, 64, a, 64, b, 64, c, 64, 2, 0) == lcg.ERR_ARG          # dtype
+    assert run(64, 64, 64, a, 64, b, 64, c, 64, 1, 9) == lcg.ERR_ARG          # algo
+    assert run(64, 64, 64, a + 2, 64, b, 64, c, 64, 1, 0) == lcg.ERR_ALIGN    # 2-byte offset
+    assert run(60, 60, 60, a, 68, b, 64, c, 64, 1, 0) == lcg.ERR_ALIGN        # ld not multiple of 8
+    assert run(64, 64, 64, a, 64, b, 64, a, 64, 1, 0) == lcg.ERR_ALIAS        # C == A
+    assert run(32, 64, 64, a, 64, b, 64, a + 32 * 64 * 2 - 16, 64, 1, 0) == lcg.ERR_ALIAS
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
