@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark: effective TFLOPS (2MNK/t) of lcgemm on the BF16 square sweep.
+
+Workload (one "step"): C = A . B for M = N = K in {2048, 4096, 8192, 16384},
+BF16 operands drawn i.i.d. N(0,1) with a seeded generator, A row-major, B
+column-major, FP32 accumulation, BF16 output, algorithm chosen per shape by
+the library's cost model (``LCGEMM_AUTO``).  ``value`` is sum(2 n^3) over the
+sweep divided by the summed device time of the four GEMMs (CUDA events on the
+launching stream, L2 flushed by a 256 MB write before every timed launch,
+outside the event pair).  ``server`` repeats the launches with seeded random
+0-5 ms host sleeps in between (the randomly spaced launch mode), ``e2e``
+times the host-buffer entry point ``lcgemm_run_host`` with page-locked inputs
+(host->device copies, the GEMM and the device->host copy of C inside the
+timed region).
+
+``--impl reference`` times the CPU oracle (FP64 triple loop, OpenMP) on a
+bounded row sample of the same workload instead.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
+the sweep (the GEMMs are independent), timing is the max over ranks and
+``value`` the flops of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SIZES = (2048, 4096, 8192, 16384)
+WORKLOAD = ("bf16 square sweep M=N=K in {2048,4096,8192,16384}; A row-major, B column-major; "
+            "entries N(0,1) seeded; FP32 accumulate, BF16 out; algo=auto")
+METRIC = "effective TFLOPS (2MNK/t) FP16/BF16 GEMM, % of GB300 dense peak, offline+server"
+UNIT = "TFLOPS"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    import torch
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, world, device):
+    import torch
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "complexity_matmul_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for p in sorted([path, os.path.join(ROOT, "complexity_matmul_gb300", "csrc", "ptx.cuh")]):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_file: str, n: int):
+    """DRAM bytes per launch from the committed ncu summary, if it still describes this source."""
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    want = _kernel_source_hash(kernel_file)
+    for fn in sorted(os.listdir(prof)):
+        if not fn.endswith(".md"):
+            continue
+        text = open(os.path.join(prof, fn)).read()
+        for m in re.finditer(r"traffic_per_launch:\s*n=(\d+)\s+bytes=(\d+)\s+source=(\w+)", text):
+            if int(m.group(1)) == n and m.group(3) == want:
+                return int(m.group(2))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons)}
+        loaded = sorted(sm)[len(sm) // 2:] if len(sm) > 4 else sm   # upper half = samples under load
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+
+    world, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    h = lcg.Handle(local)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    ops = {}
+    for n in SIZES:
+        A, B = synthetic.operands(n, n, n, "normal", 2, "bf16", str(dev))
+        C = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+        ops[n] = (A, B, C)
+    chosen = {n: lcg.ALGO_NAMES[h.select(n, n, n, lcg.BF16)] for n in SIZES}
+    launches_per_gemm = {"plain": 1, "strassen1": 2, "strassen2": 2}
+
+    def one(n, timed_events=None):
+        A, B, C = ops[n]
+        flush.fill_(1.0)                               # evict the previous launch's operands from L2
+        if timed_events is not None:
+            timed_events[0].record(stream)
+        h.run(A, B, C, algo="auto", stream=stream)
+        if timed_events is not None:
+            timed_events[1].record(stream)
+
+    for _ in range(args.warmup):
+        for n in SIZES:
+            one(n)
+    torch.cuda.synchronize(dev)
+    rc = h.sync_status()
+    if rc:
+        raise RuntimeError(f"device status {rc} after warm-up")
+
+    # ---- offline: the K timed steps
+    evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] for n in SIZES}
+    with ClockSampler(local) as clk:
+        _barrier(world)
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.perf_counter()
+        for s in range(args.steps):
+            for n in SIZES:
+                one(n, evs[n][s])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        _barrier(world)
+    rc = h.sync_status()
+    if rc:
+        raise RuntimeError(f"device status {rc} in the timed region")
+    per_n_ms = {n: [a.elapsed_time(b) for a, b in evs[n]] for n in SIZES}
+    step_ms = [sum(per_n_ms[n][s] for n in SIZES) for s in range(args.steps)]
+    total_s = _max_over_ranks(sum(step_ms) * 1e-3, world, dev)
+    flops_step = sum(2.0 * n ** 3 for n in SIZES)
+    value = flops_step * args.steps * world / total_s / 1e12
+
+    # ---- server mode: seeded random 0-5 ms host sleeps before every launch
+    rng = np.random.default_rng(1234 + rank)
+    srv = {n: [] for n in SIZES}
+    for _ in range(args.server_reps):
+        for n in SIZES:
+            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            torch.cuda.synchronize(dev)
+            time.sleep(float(rng.uniform(0.0, 5e-3)))
+            one(n, e)
+            torch.cuda.synchronize(dev)
+            srv[n].append(e[0].elapsed_time(e[1]))
+    srv_total = sum(statistics.median(srv[n]) for n in SIZES) * 1e-3
+    server_value = flops_step / srv_total / 1e12
+
+    # ---- roofline of the dominant kernel (largest share of the step)
+    peak_burst, peak_sust, hbm, peak_kind = _peaks()
+    dom = max(SIZES, key=lambda n: statistics.median(per_n_ms[n]))
+    dom_algo = chosen[dom]
+    dom_ms = statistics.mean(per_n_ms[dom])
+    mma_frac = {"plain": 1.0, "strassen1": 7 / 8, "strassen2": 49 / 64}[dom_algo]
+    achieved = mma_frac * 2.0 * dom ** 3 / (dom_ms * 1e-3) / 1e12
+    kernel_file = "gemm_plain.cu" if dom_algo == "plain" else "lcma_fused.cu"
+    traffic = _traffic(kernel_file, dom) if dom_algo == "plain" else None
+    roofline = {"bound": "tensor", "kernel": f"{dom_algo} GEMM {dom}^3", "achieved": round(achieved, 1),
+                "peak": peak_burst, "unit": "TFLOP/s", "frac": round(achieved / peak_burst, 4),
+                "peak_source": f"{peak_kind} bf16 burst", "traffic": traffic}
+
+    # ---- end to end through the host-buffer entry point (page-locked inputs)
+    e2e = run_e2e(h, ops, args, dev, stream, world)
+
+    # ---- CPU baseline: the oracle on a bounded row sample (rank 0, N = 1 only)
+    cpu = run_cpu_baseline(ops, args) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sizes": list(SIZES), "algo": "auto",
+                       "chosen": {str(n): chosen[n] for n in SIZES}, "parallelism": f"replicas x{world}",
+                       "l2": "flushed (256 MB write) before every timed launch; inputs >= 8192^3 exceed L2"},
+            "pct_of_peak": round(value / world / peak_burst, 4),
+            "per_size": {str(n): {"algo": chosen[n], "median_ms": round(statistics.median(per_n_ms[n]), 4),
+                                  "tflops": round(2.0 * n ** 3 / (statistics.median(per_n_ms[n]) * 1e-3) / 1e12, 1),
+                                  "p10_ms": round(float(np.percentile(per_n_ms[n], 10)), 4),
+                                  "p90_ms": round(float(np.percentile(per_n_ms[n], 90)), 4)} for n in SIZES},
+            "server": {"value": round(server_value, 2), "unit": UNIT, "reps": args.server_reps,
+                       "gaps_ms": "uniform 0-5, seeded"},
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": args.steps * sum(launches_per_gemm[chosen[n]] for n in SIZES),
+            "clocks": clocks,
+            "wall_s_timed": round(t_wall, 4),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(h, ops, args, dev, stream, world):
+    import ctypes
+
+    import torch
+
+    host = {}
+    for n in SIZES:
+        A, B, _ = ops[n]
+        host[n] = (A.cpu().pin_memory(), B.cpu().pin_memory(),
+                   torch.empty((n, n), dtype=torch.bfloat16).pin_memory())
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    def one(n, ev=None):
+        Ah, Bh, Ch = host[n]
+        if ev is not None:
+            ev[0].record(stream)
+        rc = h.run_host_raw(n, n, n, Ah.data_ptr(), n, Bh.data_ptr(), n, Ch.data_ptr(), n, 1, 3, sp)
+        if rc:
+            raise RuntimeError(f"lcgemm_run_host failed: {rc}")
+        if ev is not None:
+            ev[1].record(stream)
+
+    for n in SIZES:
+        one(n)
+    torch.cuda.synchronize(dev)
+    reps = max(1, min(args.steps, 3))
+    times = []
+    _barrier(world)
+    for _ in range(reps):
+        tot = 0.0
+        for n in SIZES:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            one(n, ev)
+            torch.cuda.synchronize(dev)
+            tot += ev[0].elapsed_time(ev[1]) * 1e-3
+        times.append(tot)
+    t = _max_over_ranks(statistics.median(times), world, dev)
+    flops = sum(2.0 * n ** 3 for n in SIZES)
+    return {"value": round(flops * world / t / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": sum(2 * 2 * n * n for n in SIZES),
+            "d2h_bytes_per_step": sum(2 * n * n for n in SIZES),
+            "api": "lcgemm_run_host (page-locked host buffers)"}
+
+
+def _cpu_sample_rows():
+    return 256
+
+
+def run_cpu_baseline(ops, args):
+    import numpy as np
+
+    import oracle
+    import synthetic
+    n = max(SIZES)
+    A, B, _ = ops[n]
+    rows = synthetic.row_sample(n, _cpu_sample_rows())
+    Ab = synthetic.bits(A[torch_index(rows, A.device)])
+    Bb = synthetic.bits(B)
+    t0 = time.perf_counter()
+    oracle.gemm(Ab, Bb, oracle.BF16, rows=np.arange(len(rows)))
+    t = time.perf_counter() - t0
+    flops = 2.0 * len(rows) * n * n
+    return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded rows of C for the {n}^3 GEMM (FP64 naive triple loop), {t:.1f} s"}
+
+
+def torch_index(rows, device):
+    import torch
+    return torch.as_tensor(rows, device=device)
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args):
+    import numpy as np
+
+    import oracle
+    import synthetic
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows_per = 32                      # >= the host's OpenMP threads on the GPU machine
+    data = {}
+    for n in SIZES:
+        A = synthetic.matrix(rows_per, n, "normal", 1002, "bf16")       # a row sample of A
+        B = synthetic.matrix(n, n, "normal", 2002, "bf16")
+        data[n] = (synthetic.bits(A), synthetic.bits(B))
+
+    def step():
+        for n in SIZES:
+            Ab, Bb = data[n]
+            oracle.gemm(Ab, Bb, oracle.BF16)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    flops = sum(2.0 * rows_per * n * n for n in SIZES) * args.steps
+    value = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sizes": list(SIZES), "algo": "oracle (plain definition)",
+                   "sample": f"{rows_per} rows of C per size per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows_per} rows of C for each n in {list(SIZES)} per step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_case(args):
+    """Run one GEMM shape a few times without timing (a fixed launch sequence for ncu captures)."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    dims = [int(x) for x in args.case.split(",")]
+    M, N, K = (dims * 3)[:3] if len(dims) == 1 else dims
+    dev = torch.device("cuda", 0)
+    h = lcg.Handle(0)
+    A, B = synthetic.operands(M, N, K, "normal", 2, "bf16", str(dev))
+    C = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :N]
+    for _ in range(args.reps):
+        h.run(A, B, C, algo=args.algo)
+    torch.cuda.synchronize(dev)
+    rc = h.sync_status()
+    print(f"case {M}x{N}x{K} algo={args.algo} reps={args.reps} last={lcg.ALGO_NAMES[h.last_algo()]} status={rc}")
+    h.close()
+    if rc:
+        sys.exit(1)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["lcgemm", "reference"], default="lcgemm")
+    ap.add_argument("--server-reps", type=int, default=5)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--case", default=None, help="profiling mode: run one shape 'n' or 'M,N,K' --reps times")
+    ap.add_argument("--algo", default="auto", help="algorithm for --case")
+    ap.add_argument("--reps", type=int, default=3, help="launches for --case")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -187,7 +187,8 @@ class Handle:
         M, K = A.shape
         N = Bnk.shape[0]
         if C is None:
-            C = torch.empty((M, N), dtype=A.dtype, device=A.device)
+            # rows padded to a multiple of 8 elements: the library needs 16-byte row starts
+            C = torch.empty((M, (N + 7) // 8 * 8), dtype=A.dtype, device=A.device)[:, :N]
         if C.dtype != A.dtype or C.stride(1) != 1 or tuple(C.shape) != (M, N):
             raise ValueError("C must be M x N of the input dtype with unit column stride")
         if stream is None:

@@ -58,6 +58,20 @@ def test_ragged_integer_bit_exact(h, M, N, K, dtype):
     assert_bit_exact(_run(h, A, B), oracle_c64(A, B, dtype), dtype)
 
 
+def _padded(rows, cols, dist, seed, dtype):
+    """rows x cols view of a buffer whose rows are padded to a multiple of 8 elements."""
+    buf = synthetic.matrix(rows, (cols + 7) // 8 * 8, dist, seed, dtype, "cuda")
+    return buf[:, :cols]
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 40, 100), (5, 3, 1), (130, 70, 7), (257, 129, 65)])
+def test_k_not_multiple_of_8(h, M, N, K):
+    """K that is not a multiple of 8 (rows padded in storage): exercises the K-tail zero fill."""
+    A = _padded(M, K, "int3", 17, "bf16")
+    B = _padded(N, K, "int3", 18, "bf16")
+    assert_bit_exact(_run(h, A, B), oracle_c64(A.contiguous(), B.contiguous(), "bf16"), "bf16")
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 257, 72), (513, 384, 520), (300, 130, 1000)])
 def test_ragged_normal(h, M, N, K):
     A, B = synthetic.operands(M, N, K, "normal", 8, "bf16", "cuda")
