@@ -107,7 +107,7 @@ def _traffic(kernel_file: str, n: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -122,7 +122,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -193,18 +193,17 @@ def run_gpu(args):
         if timed_events is not None:
             timed_events[1].record(stream)
 
-    for _ in range(args.warmup):
-        for n in SIZES:
-            one(n)
-    torch.cuda.synchronize(dev)
-    rc = h.sync_status()
-    if rc:
-        raise RuntimeError(f"device status {rc} after warm-up")
-
-    # ---- offline: the K timed steps
     evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for n in SIZES}
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk:          # runs through warm-up and the timed region (samples under load)
+        for _ in range(args.warmup):
+            for n in SIZES:
+                one(n)
+        torch.cuda.synchronize(dev)
+        rc = h.sync_status()
+        if rc:
+            raise RuntimeError(f"device status {rc} after warm-up")
+        # ---- offline: the K timed steps
         _barrier(world)
         torch.cuda.synchronize(dev)
         t_wall0 = time.perf_counter()
@@ -331,7 +330,7 @@ def run_e2e(h, ops, args, dev, stream, world):
 
 
 def _cpu_sample_rows():
-    return 256
+    return 1024
 
 
 def run_cpu_baseline(ops, args):
@@ -426,7 +425,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["lcgemm", "reference"], default="lcgemm")
     ap.add_argument("--server-reps", type=int, default=5)
