@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace lcg {
@@ -33,5 +34,68 @@ constexpr int kPlainBM = 128;
 constexpr int kPlainBK = 64;
 
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream);
+
+// ---------------------------------------------------------------- LCMA pre-pass / recombination
+
+// One operand side of the Combine-A/B pre-pass.  The raw operand is stored as
+// G*rows_b rows of G*kb contiguous elements (A: M x K; B: N x K).  Summed
+// operands go to dst + slot * slot_stride, rows_b rows of kb elements, dst_ld apart.
+struct CombineSide {
+  const uint16_t* src;
+  int64_t ld;
+  uint16_t* dst;
+  int64_t dst_ld;
+  int64_t slot_stride;
+  int64_t rows_b;
+  int64_t kb;      // multiple of 8
+  int64_t vecs;    // rows_b * kb / 8
+};
+struct CombineArgs {
+  CombineSide side[2];  // 0: A, 1: B
+};
+cudaError_t launch_combine_ab(const CombineArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st);
+
+// Recombination of FP32 products [R][mb][ldp] into the G x G blocks of C.
+struct CombineHArgs {
+  const float* prod;
+  int64_t ldp;
+  uint16_t* C;
+  int64_t ldc;
+  int mb, nb;
+};
+cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- fused LCMA product kernel
+
+// Where product p's operand tile comes from: a workspace slot of summed
+// operands (3-D map: k, row, slot) or one raw block of A / B in place (4-D
+// map: k, storage column block c, row, storage row block r).
+struct LcmaOperand {
+  int slot;   // >= 0: workspace slot; -1: raw block (r, c)
+  int r, c;
+};
+
+struct LcmaArgs {
+  void* C;
+  int64_t ldc;
+  int mb, nb, kb;                 // block sizes M/G, N/G, K/G
+  int tiles_m, tiles_n, num_groups, group_m;
+  LcmaOperand a_src[49], b_src[49];
+  float* prod;                    // unfused path: FP32 products [num_products][mb][ldp]
+  int64_t ldp;
+  int num_products;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+struct LcmaLaunch {
+  CUtensorMap tmA_sum, tmA_raw, tmB_sum, tmB_raw;
+  LcmaArgs args;
+  int levels;
+  bool bf16;
+  int grid;
+};
+cudaError_t launch_lcma_fused(const LcmaLaunch& L, cudaStream_t st);
+cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st);
 
 }  // namespace lcg

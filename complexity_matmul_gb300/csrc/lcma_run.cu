@@ -1,0 +1,120 @@
+// Host side of the LCMA path: workspace, the Combine-A/B pre-pass and the
+// product kernels for one- and two-level Strassen.
+#include <algorithm>
+#include <cstdint>
+
+#include "kernels.h"
+#include "lcgemm.h"
+#include "lcma_tables.h"
+#include "runtime.h"
+
+namespace lcg {
+
+namespace {
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st) {
+  if (bytes <= h->ws_bytes) return LCGEMM_OK;
+  if (h->ws) {
+    cudaStreamSynchronize(st);
+    cudaFree(h->ws);
+    h->ws = nullptr;
+    h->ws_bytes = 0;
+  }
+  if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
+    h->ws = nullptr;
+    cudaGetLastError();
+    return LCGEMM_ERR_NOMEM;
+  }
+  h->ws_bytes = bytes;
+  return LCGEMM_OK;
+}
+
+template <int L>
+int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+               const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
+  constexpr LcmaPlan<L> plan{};
+  constexpr int G = plan.G;
+  const int64_t mb = M / G, nb = N / G, kb = K / G;
+  const int na = plan.side[0].nslots, nbs = plan.side[1].nslots;
+  const int64_t a_bytes = round_up(na * mb * kb * 2, 256);
+  const int64_t b_bytes = round_up(nbs * nb * kb * 2, 256);
+  const int64_t ldp = round_up(nb, 4);
+  const int64_t p_bytes = fused ? 0 : round_up(int64_t(plan.R) * mb * ldp * 4, 256);
+  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes), st);
+  if (rc) return rc;
+  uint16_t* wsA = static_cast<uint16_t*>(h->ws);
+  uint16_t* wsB = reinterpret_cast<uint16_t*>(static_cast<char*>(h->ws) + a_bytes);
+  float* prod = reinterpret_cast<float*>(static_cast<char*>(h->ws) + a_bytes + b_bytes);
+
+  // ---- Combine-A/B pre-pass
+  CombineArgs ca{};
+  ca.side[0] = CombineSide{static_cast<const uint16_t*>(A), lda, wsA, kb, mb * kb, mb, kb, mb * kb / 8};
+  ca.side[1] = CombineSide{static_cast<const uint16_t*>(B), ldb, wsB, kb, nb * kb, nb, kb, nb * kb / 8};
+  if (launch_combine_ab(ca, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+
+  // ---- products
+  LcmaLaunch ll{};
+  ll.levels = L;
+  ll.bf16 = bf16;
+  {
+    const uint64_t dA[3] = {uint64_t(kb), uint64_t(mb), uint64_t(na)};
+    const uint64_t sA[2] = {uint64_t(kb) * 2, uint64_t(mb * kb) * 2};
+    const uint32_t box3[3] = {64u, 128u, 1u};
+    if (!encode_map(&ll.tmA_sum, bf16, wsA, 3, dA, sA, box3)) return LCGEMM_ERR_CUDA;
+    const uint64_t dB[3] = {uint64_t(kb), uint64_t(nb), uint64_t(nbs)};
+    const uint64_t sB[2] = {uint64_t(kb) * 2, uint64_t(nb * kb) * 2};
+    if (!encode_map(&ll.tmB_sum, bf16, wsB, 3, dB, sB, box3)) return LCGEMM_ERR_CUDA;
+    const uint32_t box4[4] = {64u, 1u, 128u, 1u};
+    const uint64_t rA[4] = {uint64_t(kb), uint64_t(G), uint64_t(mb), uint64_t(G)};
+    const uint64_t rsA[3] = {uint64_t(kb) * 2, uint64_t(lda) * 2, uint64_t(mb * lda) * 2};
+    if (!encode_map(&ll.tmA_raw, bf16, A, 4, rA, rsA, box4)) return LCGEMM_ERR_CUDA;
+    const uint64_t rB[4] = {uint64_t(kb), uint64_t(G), uint64_t(nb), uint64_t(G)};
+    const uint64_t rsB[3] = {uint64_t(kb) * 2, uint64_t(ldb) * 2, uint64_t(nb * ldb) * 2};
+    if (!encode_map(&ll.tmB_raw, bf16, B, 4, rB, rsB, box4)) return LCGEMM_ERR_CUDA;
+  }
+  LcmaArgs& a = ll.args;
+  a.C = C;
+  a.ldc = ldc;
+  a.mb = static_cast<int>(mb);
+  a.nb = static_cast<int>(nb);
+  a.kb = static_cast<int>(kb);
+  a.tiles_m = static_cast<int>((mb + 127) / 128);
+  a.tiles_n = static_cast<int>((nb + 127) / 128);
+  a.num_groups = a.tiles_m * a.tiles_n;
+  a.group_m = 16;
+  for (int p = 0; p < plan.R; ++p) {
+    // A is stored by (block row, block column); B (K x N stored N x K) by (N block, K block)
+    const auto& sa = plan.side[0];
+    const auto& sb = plan.side[1];
+    a.a_src[p] = sa.slot[p] >= 0 ? LcmaOperand{sa.slot[p], 0, 0} : LcmaOperand{-1, sa.alias_r[p], sa.alias_c[p]};
+    a.b_src[p] = sb.slot[p] >= 0 ? LcmaOperand{sb.slot[p], 0, 0} : LcmaOperand{-1, sb.alias_c[p], sb.alias_r[p]};
+  }
+  a.prod = prod;
+  a.ldp = ldp;
+  a.num_products = plan.R;
+  a.err = h->err_dev;
+  a.timeout_ns = h->timeout_ns;
+  if (fused) {
+    ll.grid = std::min(a.num_groups, grid_cap(h));
+    if (launch_lcma_fused(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    return LCGEMM_OK;
+  }
+  ll.grid = std::min(a.num_groups * plan.R, grid_cap(h));
+  if (launch_lcma_products(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  CombineHArgs ch{prod, ldp, static_cast<uint16_t*>(C), ldc, static_cast<int>(mb), static_cast<int>(nb)};
+  if (launch_combine_h(ch, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  return LCGEMM_OK;
+}
+
+}  // namespace
+
+int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, int64_t K, const void* A,
+                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
+  if (levels == 1) return run_levels<1>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+  if (levels == 2) return run_levels<2>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+  return LCGEMM_ERR_UNSUPPORTED;
+}
+
+}  // namespace lcg

@@ -18,14 +18,18 @@
 
 namespace lcg {
 
+// Strassen splits every dimension into 2 (4) equal blocks; the block width
+// along K must keep 16-byte row starts for the tensor-memory-access engine.
 bool algo_supported(int algo, int64_t M, int64_t N, int64_t K) {
   switch (algo) {
     case LCGEMM_PLAIN:
       return true;
+    case LCGEMM_STRASSEN1:
+    case LCGEMM_STRASSEN1_UNFUSED:
+      return M >= 2 && N >= 2 && K >= 16 && M % 2 == 0 && N % 2 == 0 && K % 16 == 0;
+    case LCGEMM_STRASSEN2:
+      return M >= 4 && N >= 4 && K >= 32 && M % 4 == 0 && N % 4 == 0 && K % 32 == 0;
     default:
-      (void)M;
-      (void)N;
-      (void)K;
       return false;
   }
 }
@@ -83,6 +87,12 @@ int dispatch(lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, const voi
   switch (algo) {
     case LCGEMM_PLAIN:
       return run_plain(h, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+    case LCGEMM_STRASSEN1:
+      return run_strassen(h, 1, true, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+    case LCGEMM_STRASSEN1_UNFUSED:
+      return run_strassen(h, 1, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+    case LCGEMM_STRASSEN2:
+      return run_strassen(h, 2, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
     default:
       return LCGEMM_ERR_UNSUPPORTED;
   }

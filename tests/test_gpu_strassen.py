@@ -1,0 +1,189 @@
+"""Parity of the Strassen (LCMA) paths against the CPU oracle (GPU, through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import complexity_matmul_gb300 as lcg
+import oracle
+import synthetic
+from helpers import assert_bit_exact, assert_close, errors, oracle_c64
+
+pytestmark = pytest.mark.gpu
+
+STRASSEN = ["strassen1", "strassen1_unfused", "strassen2"]
+
+
+@pytest.fixture(scope="module")
+def h():
+    handle = lcg.Handle(0)
+    yield handle
+    handle.close()
+
+
+def _run(h, A, B, algo):
+    C = h.run(A, B, algo=algo)
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    assert h.last_algo() == lcg.ALGOS[algo]
+    return C
+
+
+# ---------------------------------------------------------------- 256^3 FP16 (small square workload)
+
+@pytest.mark.parametrize("algo", STRASSEN)
+@pytest.mark.parametrize("dist", ["int3", "binary"])
+def test_small_square_integer_bit_exact(h, algo, dist):
+    # {-3..3}, K = 256: operand sums <= 12 in magnitude, C-block sums < 2^24 -> exact everywhere
+    A, B = synthetic.operands(256, 256, 256, dist, 1, "f16", "cuda")
+    assert_bit_exact(_run(h, A, B, algo), oracle_c64(A, B, "f16"), "f16")
+
+
+@pytest.mark.parametrize("algo", STRASSEN)
+def test_small_square_uniform(h, algo):
+    A, B = synthetic.operands(256, 256, 256, "uniform", 1, "f16", "cuda")
+    assert_close(_run(h, A, B, algo), oracle_c64(A, B, "f16"), "f16", algo)
+
+
+@pytest.mark.parametrize("algo", STRASSEN)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_integer_bit_exact_k1024(h, algo, dtype):
+    A, B = synthetic.operands(512, 768, 1024, "int3", 3, dtype, "cuda")
+    assert_bit_exact(_run(h, A, B, algo), oracle_c64(A, B, dtype), dtype)
+
+
+# ---------------------------------------------------------------- ragged block sizes
+
+RAGGED = [(258, 390, 160), (4, 4, 32), (132, 68, 64), (300, 516, 96), (1000, 24, 544), (68, 1028, 32)]
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+@pytest.mark.parametrize("algo", STRASSEN)
+def test_ragged_integer_bit_exact(h, M, N, K, algo):
+    A, B = synthetic.operands(M, N, K, "int3", 4, "bf16", "cuda")
+    assert_bit_exact(_run(h, A, B, algo), oracle_c64(A, B, "bf16"), "bf16")
+
+
+def test_strided_operands(h):
+    M, N, K = 256, 192, 320
+    Abig = synthetic.matrix(M, 400, "int3", 5, "bf16", "cuda")
+    Bbig = synthetic.matrix(N, 336, "int3", 6, "bf16", "cuda")
+    Cbig = torch.full((M, 264), 7.0, dtype=torch.bfloat16, device="cuda")
+    A, B, C = Abig[:, 16:16 + K], Bbig[:, :K], Cbig[:, 8:8 + N]
+    for algo in STRASSEN:
+        h.run(A, B, C, algo=algo)
+        torch.cuda.synchronize()
+        assert_bit_exact(C, oracle_c64(A.contiguous(), B.contiguous(), "bf16"), "bf16")
+        assert (Cbig[:, :8] == 7).all() and (Cbig[:, 8 + N:] == 7).all()
+
+
+# ---------------------------------------------------------------- square sweep and large rectangles (BF16 N(0,1))
+
+@pytest.mark.parametrize("algo", STRASSEN)
+def test_square_2048_full(h, algo):
+    A, B = synthetic.operands(2048, 2048, 2048, "normal", 2, "bf16", "cuda")
+    assert_close(_run(h, A, B, algo), oracle_c64(A, B, "bf16"), "bf16", algo)
+
+
+@pytest.mark.parametrize("n", [4096, 8192])
+@pytest.mark.parametrize("algo", ["strassen1", "strassen2"])
+def test_square_sampled_rows(h, n, algo):
+    A, B = synthetic.operands(n, n, n, "normal", 2, "bf16", "cuda")
+    C = _run(h, A, B, algo)
+    rows = synthetic.row_sample(n, 64)
+    assert_close(C, oracle_c64(A, B, "bf16", rows=rows), "bf16", algo, rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", [(16384, 16384, 8192), (8192, 28672, 8192), (32768, 8192, 4096)])
+def test_large_rectangular_error_growth(h, M, N, K):
+    """Error against FP64 on a seeded 256-row sample grows with the Strassen level but stays in tolerance."""
+    A, B = synthetic.operands(M, N, K, "normal", 5, "bf16", "cuda")
+    rows = synthetic.row_sample(M, 256, seed=5)
+    ref = oracle_c64(A, B, "bf16", rows=rows)
+    err = {}
+    for algo in ["plain", "strassen1", "strassen2"]:
+        C = _run(h, A, B, algo)
+        err[algo] = assert_close(C, ref, "bf16", algo, rows=rows)[0]
+        del C
+    assert err["plain"] <= err["strassen1"] * 1.05 + 1e-4
+    print("normwise error per level:", {k: f"{v:.3e}" for k, v in err.items()})
+
+
+# ---------------------------------------------------------------- against the dtype-emulating Strassen oracle
+
+@pytest.mark.parametrize("levels,algo", [(1, "strassen1"), (2, "strassen2"), (1, "strassen1_unfused")])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_matches_emulating_oracle(h, levels, algo, dtype):
+    """The GPU forms the summed operands exactly like the oracle's emulating Strassen
+    (FP32 sums in ascending block order, one rounding to the input type); after the one
+    final rounding the two agree element-wise except for rare one-ulp flips caused by
+    FP32 (GPU) versus FP64 (oracle) accumulation of the products."""
+    dt = oracle.F16 if dtype == "f16" else oracle.BF16
+    M, N, K = 512, 512, 1024
+    A, B = synthetic.operands(M, N, K, "normal", 6, dtype, "cuda")
+    Ab, Bb = synthetic.bits(A), synthetic.bits(B)
+    C64 = oracle.gemm(Ab, Bb, dt)
+    emu = oracle.strassen.strassen(oracle.decode(Ab, dt), oracle.decode(Bb, dt).T, levels, "emulate", dt)
+    emu_r = oracle.rounding.rne_values(emu, dt)
+    got = _run(h, A, B, algo).cpu().double().numpy()
+    to_exact = np.linalg.norm(got - C64) / np.linalg.norm(C64)
+    to_emul = np.linalg.norm(got - emu_r) / np.linalg.norm(C64)
+    assert (got == emu_r).mean() > 0.95
+    assert to_emul < 0.25 * to_exact
+
+
+# ---------------------------------------------------------------- identities, fusion and edge cases
+
+@pytest.mark.parametrize("algo", STRASSEN)
+def test_identity_on_integer_inputs(h, algo):
+    n = 256
+    A = synthetic.matrix(n, n, "int3", 7, "bf16", "cuda")
+    eye = torch.eye(n, dtype=torch.bfloat16, device="cuda")
+    assert torch.equal(_run(h, A, eye, algo), A)
+
+
+def test_fused_at_least_as_accurate_as_unfused(h):
+    A, B = synthetic.operands(1024, 1024, 2048, "normal", 8, "bf16", "cuda")
+    C64 = oracle_c64(A, B, "bf16")
+    e_f = errors(_run(h, A, B, "strassen1"), C64)[0]
+    e_u = errors(_run(h, A, B, "strassen1_unfused"), C64)[0]
+    assert e_f <= e_u * 1.02
+
+
+def test_unsupported_dimensions(h):
+    A = synthetic.matrix(130, 72, "int3", 9, "bf16", "cuda")
+    B = synthetic.matrix(66, 72, "int3", 10, "bf16", "cuda")
+    C = torch.empty((130, 72), dtype=torch.bfloat16, device="cuda")[:, :66]
+    stream = torch.cuda.current_stream().cuda_stream
+    import ctypes
+    sp = ctypes.c_void_p(stream)
+    # K = 72 is not a multiple of 16 (strassen1) / 32 (strassen2)
+    for algo in ("strassen1", "strassen2", "strassen1_unfused"):
+        rc = h.run_raw(130, 66, 72, A.data_ptr(), 72, B.data_ptr(), 72, C.data_ptr(), 72, lcg.BF16,
+                       lcg.ALGOS[algo], sp)
+        assert rc == lcg.ERR_UNSUPPORTED
+    # M = 130 is not a multiple of 4 (strassen2) even with a valid K
+    A2 = synthetic.matrix(130, 64, "int3", 9, "bf16", "cuda")
+    B2 = synthetic.matrix(66, 64, "int3", 10, "bf16", "cuda")
+    assert h.run_raw(130, 66, 64, A2.data_ptr(), 64, B2.data_ptr(), 64, C.data_ptr(), 72, lcg.BF16,
+                     lcg.STRASSEN2, sp) == lcg.ERR_UNSUPPORTED
+    # auto never fails: it falls back to plain
+    h.run(A, B, C, algo="auto")
+    torch.cuda.synchronize()
+    assert h.last_algo() == lcg.PLAIN
+    assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
+
+
+def test_repeated_and_interleaved_launches(h):
+    """Workspace reuse and growth across shapes and algorithms, many launches in a row."""
+    shapes = [(512, 512, 512), (1024, 768, 256), (256, 256, 2048)]
+    data = [synthetic.operands(M, N, K, "int3", 11 + i, "f16", "cuda") for i, (M, N, K) in enumerate(shapes)]
+    refs = [oracle_c64(A, B, "f16") for A, B in data]
+    outs = []
+    for _ in range(4):
+        for i, (A, B) in enumerate(data):
+            for algo in STRASSEN:
+                outs.append((i, h.run(A, B, algo=algo)))
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    for i, C in outs[-len(shapes) * len(STRASSEN):]:
+        assert_bit_exact(C, refs[i], "f16")
