@@ -53,7 +53,15 @@ def test_integer_bit_exact_k1024(h, algo, dtype):
 
 # ---------------------------------------------------------------- ragged block sizes
 
-RAGGED = [(258, 390, 160), (4, 4, 32), (132, 68, 64), (300, 516, 96), (1000, 24, 544), (68, 1028, 32)]
+RAGGED = [(260, 388, 160), (4, 4, 32), (132, 68, 64), (300, 516, 96), (1000, 24, 544), (68, 1028, 32)]
+RAGGED_S1 = [(258, 390, 160), (2, 6, 16), (130, 66, 48)]   # even, but not multiples of 4
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED_S1)
+@pytest.mark.parametrize("algo", ["strassen1", "strassen1_unfused"])
+def test_ragged_one_level_only(h, M, N, K, algo):
+    A, B = synthetic.operands(M, N, K, "int3", 4, "f16", "cuda")
+    assert_bit_exact(_run(h, A, B, algo), oracle_c64(A, B, "f16"), "f16")
 
 
 @pytest.mark.parametrize("M,N,K", RAGGED)
