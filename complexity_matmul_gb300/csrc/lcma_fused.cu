@@ -32,8 +32,8 @@
 //
 // Warp roles as in the plain kernel: warp 0 TMA producer, warp 1 TMEM owner
 // and MMA issuer, warps 2..5 epilogue (TMEM read-modify-write and stores).
-// The MMA issuer waits on an epilogue progress counter before reusing a
-// buffer; the epilogue waits on one mbarrier per product step.
+// The MMA issuer waits on per-warp epilogue progress counters before reusing
+// a buffer; the epilogue waits on one mbarrier per product step.
 #include "kernels.h"
 #include "lcma_tables.h"
 #include "ptx.cuh"
@@ -170,12 +170,20 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
-// Bounded wait until *ctr >= target.
+// The four epilogue warps advance independently (a warp with no rows inside C
+// skips its stores and runs ahead), so each keeps its own count of finished
+// ops; an op is complete once every warp's count has passed it.
+__device__ __forceinline__ bool counters_reached(const uint32_t* ctr, uint32_t target) {
+  return ld_acquire_u32(ctr) >= target && ld_acquire_u32(ctr + 1) >= target && ld_acquire_u32(ctr + 2) >= target &&
+         ld_acquire_u32(ctr + 3) >= target;
+}
+
+// Bounded wait until all four counters ctr[0..3] >= target.
 __device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t target, const WaitCtl& w) {
-  if (ld_acquire_u32(ctr) >= target) return true;
+  if (counters_reached(ctr, target)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (ld_acquire_u32(ctr) >= target) return true;
+    if (counters_reached(ctr, target)) return true;
     if ((i & 31u) == 0) {
       if (*w.abort_flag) return false;
       if (globaltimer_ns() - t0 > w.timeout_ns) {
@@ -257,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mdone = bars + 2 * kStages;          // one per program step
   uint64_t* drain = mdone + kSteps;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  uint32_t* progress = tmem_slot + 1;            // epilogue ops completed x 4 warps
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  uint32_t* progress = tmem_slot + 1;            // [4]: epilogue ops completed, per epilogue warp
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 5);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kSteps; ++s) mbar_init(&mdone[s], 1);
     mbar_init(drain, 1);
-    *progress = 0;
+    for (int w = 0; w < 4; ++w) progress[w] = 0;
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA_sum);
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; ok && t < args.num_groups; t += gridDim.x, ++g) {
         for (int s = 0; ok && s < kSteps; ++s) {
           const int need = static_cast<int>(g) * kNumOps + d_step_need[s];
-          if (need > 0 && !wait_counter(progress, 4u * static_cast<uint32_t>(need), wc)) {
+          if (need > 0 && !wait_counter(progress, static_cast<uint32_t>(need), wc)) {
             ok = false;
             break;
           }
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) red_release_add(progress, 1u);
+        if (lane == 0) red_release_add(progress + q, 1u);
       }
     }
   }
