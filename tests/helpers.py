@@ -15,8 +15,12 @@ NORMWISE_TOL = {
     ("strassen", "f16"): 4e-3,
     ("strassen", "bf16"): 1.6e-2,
 }
-# max_ij |C_gpu - C64| <= MAXERR_SIGMA * sigma_C, sigma_C = RMS(C64)
+# max_ij |C_gpu - C64| <= MAXERR_SIGMA * sigma_C, sigma_C = RMS(C64).  0.05 everywhere except
+# two-level Strassen in BF16: rounding the 4-term operand sums to BF16 alone (the oracle's
+# emulating Strassen, exact products) already reaches max/sigma_C = 0.071 on 1024^3 and
+# 2048^3 N(0,1) inputs, so that algorithm/dtype pair is held to 0.10.
 MAXERR_SIGMA = 0.05
+MAXERR_SIGMA_OVERRIDE = {("strassen2", "bf16"): 0.10}
 
 
 def family(algo: str) -> str:
@@ -60,5 +64,6 @@ def assert_close(C: torch.Tensor, C64: np.ndarray, dtype: str, algo: str, rows=N
     normwise, maxerr, sigma = errors(C, C64, rows)
     tol = NORMWISE_TOL[(family(algo), dtype)]
     assert normwise <= tol, f"normwise error {normwise:.3e} > {tol:.1e} ({algo}, {dtype})"
-    assert maxerr <= MAXERR_SIGMA * sigma, f"max error {maxerr:.3e} > {MAXERR_SIGMA} * sigma_C ({sigma:.3e})"
+    bound = MAXERR_SIGMA_OVERRIDE.get((algo, dtype), MAXERR_SIGMA)
+    assert maxerr <= bound * sigma, f"max error {maxerr:.3e} > {bound} * sigma_C ({sigma:.3e})"
     return normwise, maxerr, sigma
