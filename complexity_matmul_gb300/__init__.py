@@ -24,12 +24,13 @@ ALGOS = {"plain": PLAIN, "strassen1": STRASSEN1, "strassen2": STRASSEN2, "auto":
          "strassen1_unfused": STRASSEN1_UNFUSED}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 OK, ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM = 0, -1, -2, -3, -4, -5, -6, -7
+ERR_TOO_LARGE = -8
 OPT_WAIT_TIMEOUT_US, OPT_GROUP_ORDER, OPT_SPLIT, OPT_MAX_CTAS = 1, 2, 3, 4
 OPT_PEAK_GFLOPS, OPT_HBM_GBPS, OPT_DEBUG_DROP_SIGNAL = 5, 6, 7
 
 EXPORTS = ("lcgemm_create", "lcgemm_destroy", "lcgemm_run", "lcgemm_run_host", "lcgemm_last_algo",
            "lcgemm_select", "lcgemm_estimate", "lcgemm_sync_status", "lcgemm_set_option",
-           "lcgemm_strerror")
+           "lcgemm_strerror", "lcgemm_strassen1_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,7 @@ def lib(build_if_missing: bool = False):
         L.lcgemm_estimate.argtypes = [vp, i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_double)]
         L.lcgemm_sync_status.argtypes = [vp, vp]
         L.lcgemm_set_option.argtypes = [vp, i32, i64]
+        L.lcgemm_strassen1_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp]
         L.lcgemm_strerror.argtypes = [i32]
         L.lcgemm_strerror.restype = ctypes.c_char_p
         for name in EXPORTS:

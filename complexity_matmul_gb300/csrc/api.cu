@@ -357,6 +357,7 @@ const char* lcgemm_strerror(int code) {
     case LCGEMM_ERR_CUDA: return "CUDA call or kernel launch failed";
     case LCGEMM_ERR_TIMEOUT: return "a bounded device-side wait gave up in an earlier launch";
     case LCGEMM_ERR_NOMEM: return "workspace allocation failed";
+    case LCGEMM_ERR_TOO_LARGE: return "problem too large for the fixed scratch of lcgemm_strassen1_noalloc";
     default: return "unknown status code";
   }
 }

@@ -83,7 +83,8 @@ enum {
   LCGEMM_ERR_ALIAS = -4,        /* C overlaps A or B                                      */
   LCGEMM_ERR_CUDA = -5,         /* a CUDA runtime/driver call or launch failed            */
   LCGEMM_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up (earlier launch)    */
-  LCGEMM_ERR_NOMEM = -7         /* workspace or staging allocation failed                 */
+  LCGEMM_ERR_NOMEM = -7,        /* workspace or staging allocation failed                 */
+  LCGEMM_ERR_TOO_LARGE = -8     /* problem exceeds lcgemm_strassen1_noalloc's fixed scratch */
 };
 
 /* options for lcgemm_set_option */
@@ -147,6 +148,34 @@ LCGEMM_API int lcgemm_sync_status(lcgemm_t h, void* cuda_stream);
 
 /* Set an LCGEMM_OPT_* option.  Returns LCGEMM_ERR_ARG for unknown keys or bad values. */
 LCGEMM_API int lcgemm_set_option(lcgemm_t h, int option, int64_t value);
+
+/*
+ * One-level Strassen (the same kernels as LCGEMM_STRASSEN1) that allocates
+ * nothing.  The paper has no counterpart to this entry point.
+ *
+ * For callers that must not allocate device memory while they run -- a
+ * framework whose caching allocator already owns the device's memory, so a
+ * cudaMalloc from a library would compete for the same pool, or a service or
+ * safety-critical process that only allocates at start-up.  It needs no
+ * handle; its scratch (the summed operand blocks) is a fixed 16 MiB array that
+ * every device holds from the moment the library is loaded until the process
+ * exits, and the call makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * Arguments, layouts and alignment rules are those of lcgemm_run; requires M,
+ * N even and K a multiple of 16 (else LCGEMM_ERR_UNSUPPORTED).  The summed
+ * operands take 2.5 * K * (M + N) bytes plus alignment; larger problems fail
+ * with LCGEMM_ERR_TOO_LARGE (e.g. M = N = K = 1792 fits, 2048 does not).
+ * Runs asynchronously on `cuda_stream`.  All calls on a device share the one
+ * array: calls that overlap on the GPU (other streams, other threads) race and
+ * must be serialised by the caller.  The array keeps the previous call's data;
+ * its error word is cleared on every call.  Bounded device-side waits still
+ * end the kernel if they run out, but this entry point does not report them.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ */
+LCGEMM_API int lcgemm_strassen1_noalloc(int64_t M, int64_t N, int64_t K,
+                                        const void* A, int64_t lda, const void* B, int64_t ldb,
+                                        void* C, int64_t ldc, int dtype, void* cuda_stream);
 
 /* Static description of a status code (never NULL). */
 LCGEMM_API const char* lcgemm_strerror(int code);
