@@ -133,27 +133,40 @@ int grid_cap(const lcgemm_ctx* h) {
   return h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms;
 }
 
+// Single-CTA 128 x 256 tiles or CTA-pair 256 x 256 tiles (see gemm_pair.cu).
+int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N) {
+  if (grid_cap(h) < 2) return 1;
+  if (h->plain_kernel == 1 || h->plain_kernel == 2) return h->plain_kernel;
+  return (M > 128 && N > 128) ? 2 : 1;
+}
+
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
   PlainLaunch L{};
   L.bf16 = bf16;
-  L.bn = N <= 128 ? 128 : 256;
+  const bool pair = plain_variant(h, M, N) == 2;
+  const int bm = pair ? 2 * kPlainBM : kPlainBM;
+  L.bn = pair ? 256 : (N <= 128 ? 128 : 256);
   if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, kPlainBM)) return LCGEMM_ERR_CUDA;
-  if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, L.bn)) return LCGEMM_ERR_CUDA;
+  if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, pair ? L.bn / 2 : L.bn)) return LCGEMM_ERR_CUDA;
   PlainArgs& a = L.args;
   a.C = C;
   a.ldc = ldc;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.tiles_m = static_cast<int>((M + kPlainBM - 1) / kPlainBM);
+  a.tiles_m = static_cast<int>((M + bm - 1) / bm);
   a.tiles_n = static_cast<int>((N + L.bn - 1) / L.bn);
   const int64_t tiles = int64_t(a.tiles_m) * a.tiles_n;
   if (tiles > kMaxDim) return LCGEMM_ERR_UNSUPPORTED;
   a.num_tiles = static_cast<int>(tiles);
-  a.group_m = 16;
+  a.group_m = pair ? 8 : 16;
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
+  if (pair) {
+    L.grid = 2 * static_cast<int>(std::min<int64_t>(tiles, grid_cap(h) / 2));
+    return launch_plain_pair(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+  }
   L.grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap(h)));
   return launch_plain(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
 }
@@ -341,6 +354,10 @@ int lcgemm_set_option(lcgemm_t h, int option, int64_t value) {
     case LCGEMM_OPT_DEBUG_DROP_SIGNAL:
       if (value != 0 && value != 1) return LCGEMM_ERR_ARG;
       h->debug_drop = static_cast<int>(value);
+      return LCGEMM_OK;
+    case LCGEMM_OPT_PLAIN_KERNEL:
+      if (value < 0 || value > 2) return LCGEMM_ERR_ARG;
+      h->plain_kernel = static_cast<int>(value);
       return LCGEMM_OK;
     default:
       return LCGEMM_ERR_ARG;

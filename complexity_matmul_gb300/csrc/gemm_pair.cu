@@ -1,0 +1,246 @@
+// Plain GEMM on CTA pairs (cta_group::2): 256 x 256 output tiles per pair.
+//
+// Same pipeline as the single-CTA kernel (TMA producer, MMA issuer, four
+// epilogue warps, two TMEM accumulators), but each tcgen05.mma covers M = 256
+// rows: the even CTA of a cluster of two issues it, each CTA stages 128 rows
+// of A and 128 of the 256 B rows in its own shared memory, and each CTA keeps
+// its 128 accumulator rows in its own tensor memory.  Per SM the tensor core
+// reads 16 KB of A and 8 KB of (its half of) B per 64-deep K slab instead of
+// 16 KB + 32 KB, which halves the shared-memory and L2 traffic per flop.
+//
+// Synchronisation across the pair:
+//   full[s]   leader's barrier; the leader arms it with both CTAs' bytes and
+//             both CTAs' TMA copies complete on it
+//   empty[s]  one per CTA; the leader's MMA commit arrives on both
+//   tfull[b]  one per CTA; the leader's MMA commit arrives on both
+//   tempty[b] leader's barrier; all 8 epilogue warps of the pair arrive
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lcg {
+
+namespace {
+
+constexpr int kBM = 128;           // rows per CTA (256 per pair)
+constexpr int kBN = 256;           // columns per pair (128 B rows staged per CTA)
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kThreads = 192;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = (kBN / 2) * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTxBytes = 2 * kStageBytes;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+
+__device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& mb, int& nb) {
+  const int group_tiles = a.group_m * a.tiles_n;
+  const int g = tile / group_tiles;
+  const int first_m = g * a.group_m;
+  const int rows = min(a.tiles_m - first_m, a.group_m);
+  const int local = tile - g * group_tiles;
+  mb = first_m + local % rows;
+  nb = local / rows;
+}
+
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    plain_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const PlainArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
+  const int num_kb = (args.K + kBK - 1) / kBK;
+  const int pair = blockIdx.x / 2;
+  const int num_pairs = gridDim.x / 2;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs) {
+        int mb, nb;
+        tile_coords(tile, args, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], kTxBytes);
+          const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+          tma_load_2d_pair(sA + stage * kABytes, &tmA, bar, kb * kBK, mb * 2 * kBM + rank * kBM);
+          tma_load_2d_pair(sB + stage * kBBytes, &tmB, bar, kb * kBK, nb * kBN + rank * (kBN / 2));
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // Aborting: let this CTA's copies land before it leaves.
+        if (leader)
+          for (int s = 0; s < kStages; ++s)
+            if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, wc, false);
+        settle_ns(1000000);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_f16(BF16, 2 * kBM, kBN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_f16_pair(d_tmem, sdesc_k128(a0 + k * 32), sdesc_k128(b0 + k * 32), idesc, (kb | k) != 0);
+          mma_commit_pair(&empty[stage]);
+          issued = true;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok && issued) {
+        mma_commit_pair(drain);
+        mbar_wait(drain, 0, wc, false);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    uint16_t* Cp = static_cast<uint16_t*>(args.C);
+    for (int tile = pair; tile < args.num_tiles; tile += num_pairs) {
+      int mb, nb;
+      tile_coords(tile, args, mb, nb);
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc))) break;
+      tc_fence_after();
+      const int row = mb * 2 * kBM + rank * kBM + q * 32 + lane;
+      uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c * 32, r);
+        tmem_wait_ld();
+        const int col = nb * kBN + c * 32;
+        if (row < args.M && col < args.N) {
+          if (col + 32 <= args.N) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
+              o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
+              o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
+              o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
+              dst[v] = o;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
+              if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
+              if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
+  auto kern = plain_pair_kernel<BF16>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<L.grid, kThreads, kSmemBytes, stream>>>(L.tmA, L.tmB, L.args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream) {
+  if (L.grid % 2) return cudaErrorInvalidValue;
+  return L.bf16 ? launch_impl<true>(L, stream) : launch_impl<false>(L, stream);
+}
+
+}  // namespace lcg

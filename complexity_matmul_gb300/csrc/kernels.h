@@ -34,6 +34,8 @@ constexpr int kPlainBM = 128;
 constexpr int kPlainBK = 64;
 
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream);
+// CTA-pair variant: 256 x 256 tiles per cluster of two; tensor maps use 128-row boxes for A and B.
+cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 
 // ---------------------------------------------------------------- LCMA pre-pass / recombination
 

@@ -16,6 +16,7 @@ struct lcgemm_ctx {
   int split = 1;
   int max_ctas = 0;
   int debug_drop = 0;
+  int plain_kernel = 0;         // 0: choose, 1: single-CTA 128 x 256 tiles, 2: CTA-pair 256 x 256 tiles
   double peak_gflops = 2.25e6;  // dense FP16/BF16 tensor peak (GFLOP/s)
   double hbm_gbps = 8000.0;     // HBM bandwidth (GB/s)
   int last_algo = -1;

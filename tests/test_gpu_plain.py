@@ -12,9 +12,11 @@ from helpers import assert_bit_exact, assert_close, oracle_c64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def h():
+@pytest.fixture(scope="module", params=[1, 2], ids=["single_cta", "cta_pair"])
+def h(request):
+    """Every plain test runs on both kernels: single-CTA 128x256 tiles and CTA-pair 256x256 tiles."""
     handle = lcg.Handle(0)
+    handle.set_option(lcg.OPT_PLAIN_KERNEL, request.param)
     yield handle
     handle.close()
 
