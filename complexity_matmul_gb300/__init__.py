@@ -26,7 +26,7 @@ ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 OK, ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM = 0, -1, -2, -3, -4, -5, -6, -7
 ERR_TOO_LARGE = -8
 OPT_WAIT_TIMEOUT_US, OPT_GROUP_ORDER, OPT_SPLIT, OPT_MAX_CTAS = 1, 2, 3, 4
-OPT_PEAK_GFLOPS, OPT_HBM_GBPS, OPT_DEBUG_DROP_SIGNAL, OPT_PLAIN_KERNEL = 5, 6, 7, 8
+OPT_PEAK_GFLOPS, OPT_HBM_GBPS, OPT_DEBUG_DROP_SIGNAL, OPT_PLAIN_KERNEL, OPT_LCMA_KERNEL = 5, 6, 7, 8, 9
 
 EXPORTS = ("lcgemm_create", "lcgemm_destroy", "lcgemm_run", "lcgemm_run_host", "lcgemm_last_algo",
            "lcgemm_select", "lcgemm_estimate", "lcgemm_sync_status", "lcgemm_set_option",

@@ -99,5 +99,7 @@ struct LcmaLaunch {
 };
 cudaError_t launch_lcma_fused(const LcmaLaunch& L, cudaStream_t st);
 cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st);
+// CTA-pair fused one-level kernel: Groups of 256 x 128 quadrant tiles; B maps use 64-row boxes.
+cudaError_t launch_lcma_pair(const LcmaLaunch& L, cudaStream_t st);
 
 }  // namespace lcg

@@ -55,24 +55,30 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   if (launch_combine_ab(ca, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
 
   // ---- products
+  // fused one-level Groups run on CTA pairs (256 x 128 tiles) unless the quadrant is small
+  const bool pair = fused && L == 1 && grid_cap(h) >= 2 &&
+                    (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
+  const int b_box = pair ? 64 : 128;
   LcmaLaunch ll{};
   ll.levels = L;
   ll.bf16 = bf16;
   {
     const uint64_t dA[3] = {uint64_t(kb), uint64_t(mb), uint64_t(na)};
     const uint64_t sA[2] = {uint64_t(kb) * 2, uint64_t(mb * kb) * 2};
-    const uint32_t box3[3] = {64u, 128u, 1u};
-    if (!encode_map(&ll.tmA_sum, bf16, wsA, 3, dA, sA, box3)) return LCGEMM_ERR_CUDA;
+    const uint32_t boxA3[3] = {64u, 128u, 1u};
+    const uint32_t boxB3[3] = {64u, uint32_t(b_box), 1u};
+    if (!encode_map(&ll.tmA_sum, bf16, wsA, 3, dA, sA, boxA3)) return LCGEMM_ERR_CUDA;
     const uint64_t dB[3] = {uint64_t(kb), uint64_t(nb), uint64_t(nbs)};
     const uint64_t sB[2] = {uint64_t(kb) * 2, uint64_t(nb * kb) * 2};
-    if (!encode_map(&ll.tmB_sum, bf16, wsB, 3, dB, sB, box3)) return LCGEMM_ERR_CUDA;
-    const uint32_t box4[4] = {64u, 1u, 128u, 1u};
+    if (!encode_map(&ll.tmB_sum, bf16, wsB, 3, dB, sB, boxB3)) return LCGEMM_ERR_CUDA;
+    const uint32_t boxA4[4] = {64u, 1u, 128u, 1u};
+    const uint32_t boxB4[4] = {64u, 1u, uint32_t(b_box), 1u};
     const uint64_t rA[4] = {uint64_t(kb), uint64_t(G), uint64_t(mb), uint64_t(G)};
     const uint64_t rsA[3] = {uint64_t(kb) * 2, uint64_t(lda) * 2, uint64_t(mb * lda) * 2};
-    if (!encode_map(&ll.tmA_raw, bf16, A, 4, rA, rsA, box4)) return LCGEMM_ERR_CUDA;
+    if (!encode_map(&ll.tmA_raw, bf16, A, 4, rA, rsA, boxA4)) return LCGEMM_ERR_CUDA;
     const uint64_t rB[4] = {uint64_t(kb), uint64_t(G), uint64_t(nb), uint64_t(G)};
     const uint64_t rsB[3] = {uint64_t(kb) * 2, uint64_t(ldb) * 2, uint64_t(nb * ldb) * 2};
-    if (!encode_map(&ll.tmB_raw, bf16, B, 4, rB, rsB, box4)) return LCGEMM_ERR_CUDA;
+    if (!encode_map(&ll.tmB_raw, bf16, B, 4, rB, rsB, boxB4)) return LCGEMM_ERR_CUDA;
   }
   LcmaArgs& a = ll.args;
   a.C = C;
@@ -80,7 +86,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   a.mb = static_cast<int>(mb);
   a.nb = static_cast<int>(nb);
   a.kb = static_cast<int>(kb);
-  a.tiles_m = static_cast<int>((mb + 127) / 128);
+  a.tiles_m = static_cast<int>(pair ? (mb + 255) / 256 : (mb + 127) / 128);
   a.tiles_n = static_cast<int>((nb + 127) / 128);
   a.num_groups = a.tiles_m * a.tiles_n;
   a.group_m = 16;
@@ -96,6 +102,11 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   a.num_products = plan.R;
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
+  if (pair) {
+    ll.grid = 2 * std::min(a.num_groups, grid_cap(h) / 2);
+    if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    return LCGEMM_OK;
+  }
   if (fused) {
     ll.grid = std::min(a.num_groups, grid_cap(h));
     if (launch_lcma_fused(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;

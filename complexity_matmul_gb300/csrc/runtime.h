@@ -17,6 +17,7 @@ struct lcgemm_ctx {
   int max_ctas = 0;
   int debug_drop = 0;
   int plain_kernel = 0;         // 0: choose, 1: single-CTA 128 x 256 tiles, 2: CTA-pair 256 x 256 tiles
+  int lcma_kernel = 0;          // fused one-level: 0 choose, 1 single-CTA 128 x 128 Groups, 2 CTA-pair 256 x 128
   double peak_gflops = 2.25e6;  // dense FP16/BF16 tensor peak (GFLOP/s)
   double hbm_gbps = 8000.0;     // HBM bandwidth (GB/s)
   int last_algo = -1;

@@ -13,9 +13,11 @@ pytestmark = pytest.mark.gpu
 STRASSEN = ["strassen1", "strassen1_unfused", "strassen2"]
 
 
-@pytest.fixture(scope="module")
-def h():
+@pytest.fixture(scope="module", params=[1, 2], ids=["single_cta", "cta_pair"])
+def h(request):
+    """Every Strassen test runs with both fused one-level kernels (single-CTA and CTA-pair Groups)."""
     handle = lcg.Handle(0)
+    handle.set_option(lcg.OPT_LCMA_KERNEL, request.param)
     yield handle
     handle.close()
 
