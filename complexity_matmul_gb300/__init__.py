@@ -113,8 +113,14 @@ def _algo_code(algo) -> int:
     return ALGOS[algo] if isinstance(algo, str) else int(algo)
 
 
+PLANNING_DEVICE = -1
+
+
 class Handle:
-    """Owns an ``lcgemm_t`` (workspace, error word, options) for one device."""
+    """Owns an ``lcgemm_t`` (workspace, error word, options) for one device.
+
+    ``Handle(PLANNING_DEVICE)`` answers cost-model queries without touching CUDA.
+    """
 
     def __init__(self, device: int = 0):
         self._lib = lib()

@@ -180,6 +180,15 @@ extern "C" {
 int lcgemm_create(lcgemm_t* out, int device) {
   if (!out) return LCGEMM_ERR_ARG;
   *out = nullptr;
+  if (device == LCGEMM_PLANNING_DEVICE) {
+    // cost-model queries only: no CUDA call, GB300 machine model
+    auto* h = new (std::nothrow) lcgemm_ctx();
+    if (!h) return LCGEMM_ERR_NOMEM;
+    h->device = LCGEMM_PLANNING_DEVICE;
+    h->num_sms = 152;
+    *out = h;
+    return LCGEMM_OK;
+  }
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) return LCGEMM_ERR_ARG;
   DeviceGuard g(device);
@@ -215,6 +224,10 @@ int lcgemm_create(lcgemm_t* out, int device) {
 
 int lcgemm_destroy(lcgemm_t h) {
   if (!h) return LCGEMM_OK;
+  if (h->device == LCGEMM_PLANNING_DEVICE) {
+    delete h;
+    return LCGEMM_OK;
+  }
   DeviceGuard g(h->device);
   cudaDeviceSynchronize();
   if (h->ws) cudaFree(h->ws);
@@ -226,7 +239,7 @@ int lcgemm_destroy(lcgemm_t h) {
 
 int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
-  if (!h) return LCGEMM_ERR_ARG;
+  if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;
   int rc = check_shape(M, N, K, dtype, algo);
   if (rc) return rc;
   if (M == 0 || N == 0) return LCGEMM_OK;
@@ -253,7 +266,7 @@ int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64
 
 int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
-  if (!h) return LCGEMM_ERR_ARG;
+  if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;
   int rc = check_shape(M, N, K, dtype, algo);
   if (rc) return rc;
   if (M == 0 || N == 0) return LCGEMM_OK;
@@ -315,7 +328,7 @@ int lcgemm_estimate(lcgemm_t h, int64_t M, int64_t N, int64_t K, int dtype, int 
 }
 
 int lcgemm_sync_status(lcgemm_t h, void* cuda_stream) {
-  if (!h) return LCGEMM_ERR_ARG;
+  if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;
   DeviceGuard g(h->device);
   if (!g.ok) return LCGEMM_ERR_CUDA;
   const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));

@@ -36,17 +36,31 @@ bool algo_supported(int algo, int64_t M, int64_t N, int64_t K) {
 
 namespace {
 
-// Fractions of the tensor peak and of the HBM bandwidth each kernel reaches
-// when it is not limited by its tile grid (calibrated on GB300).
-constexpr double kEtaPlain = 0.70;
-constexpr double kBetaStream = 0.85;
-constexpr double kLaunchSec = 4e-6;
+// Calibration: the fraction of the dense tensor peak each product kernel
+// sustains once its tile grid fills the machine, and the fraction of HBM
+// bandwidth the streaming kernels reach.  Measured on GB300 (1 CTA per SM).
+constexpr double kEtaPlainPair = 0.86;    // CTA-pair 256 x 256 tiles
+constexpr double kEtaPlainSingle = 0.78;  // single-CTA 128 x 256 tiles
+constexpr double kEtaLcmaPair = 0.80;     // fused one-level Groups on CTA pairs (256 x 128, 7 products)
+constexpr double kEtaLcmaSingle = 0.55;   // single-CTA 128 x 128 product tiles (shared-memory bound)
+constexpr double kBetaStream = 0.80;      // combine pre-pass / recombination, fraction of HBM bandwidth
+constexpr double kLaunchSec = 6e-6;       // launch + prologue + pipeline fill of one kernel
 
-double wave_efficiency(int64_t tiles, int sms) {
-  if (tiles <= 0) return 1.0;
-  const int64_t waves = (tiles + sms - 1) / sms;
-  return static_cast<double>(tiles) / static_cast<double>(waves * sms);
+double wave_efficiency(int64_t tiles, int units) {
+  if (tiles <= 0 || units <= 0) return 1.0;
+  const int64_t waves = (tiles + units - 1) / units;
+  return static_cast<double>(tiles) / static_cast<double>(waves * units);
 }
+
+// One kernel on the roofline: compute time at eta * peak stretched by wave
+// quantisation, or streaming time, whichever is longer, plus launch overhead.
+double kernel_time(double flops, double bytes, int64_t tiles, int units, double eta, double P, double BW) {
+  const double t_c = flops > 0 ? flops / (eta * P * wave_efficiency(tiles, units)) : 0.0;
+  const double t_m = bytes / (kBetaStream * BW);
+  return std::max(t_c, t_m) + kLaunchSec;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
@@ -55,13 +69,41 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
   const double BW = h->hbm_gbps * 1e9;
   const double m = static_cast<double>(M), n = static_cast<double>(N), k = static_cast<double>(K);
   const int sms = std::max(1, h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms);
+  const double mnk2 = 2.0 * m * n * k;
   if (algo == LCGEMM_PLAIN) {
-    const int bn = N <= 128 ? 128 : 256;
-    const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
-    const double flops = 2.0 * m * n * k;
     const double bytes = 2.0 * (m * k + k * n + m * n);
-    const double t_mma = flops / (kEtaPlain * P * wave_efficiency(tiles, sms));
-    return std::max(t_mma, bytes / (kBetaStream * BW)) + kLaunchSec;
+    const bool pair = sms >= 2 && (h->plain_kernel == 2 || (h->plain_kernel == 0 && M > 128 && N > 128));
+    if (pair) return kernel_time(mnk2, bytes, cdiv(M, 256) * cdiv(N, 256), sms / 2, kEtaPlainPair, P, BW);
+    const int64_t bn = N <= 128 ? 128 : 256;
+    return kernel_time(mnk2, bytes, cdiv(M, 128) * cdiv(N, bn), sms, kEtaPlainSingle, P, BW);
+  }
+  if (!algo_supported(algo, M, N, K)) return INFINITY;
+  if (algo == LCGEMM_STRASSEN1 || algo == LCGEMM_STRASSEN1_UNFUSED) {
+    const int64_t mb = M / 2, nb = N / 2;
+    // pre-pass: read A and B once, write 5 summed blocks of each (2 of 7 products alias raw blocks)
+    const double t_pre = kernel_time(0, 4.5 * (m * k + k * n), 0, 1, 1.0, P, BW);
+    const double flops = 7.0 / 8.0 * mnk2;
+    if (algo == LCGEMM_STRASSEN1) {
+      const double bytes = 3.5 * (m * k + k * n) + 2.0 * m * n;
+      const bool pair = sms >= 2 && (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
+      const double t = pair ? kernel_time(flops, bytes, cdiv(mb, 256) * cdiv(nb, 128), sms / 2, kEtaLcmaPair, P, BW)
+                            : kernel_time(flops, bytes, cdiv(mb, 128) * cdiv(nb, 128), sms, kEtaLcmaSingle, P, BW);
+      return t_pre + t;
+    }
+    const double t_prod = kernel_time(flops, 3.5 * (m * k + k * n) + 7.0 * m * n, 7 * cdiv(mb, 128) * cdiv(nb, 128),
+                                      sms, kEtaLcmaSingle, P, BW);
+    const double t_h = kernel_time(0, 9.0 * m * n, 0, 1, 1.0, P, BW);
+    return t_pre + t_prod + t_h;
+  }
+  if (algo == LCGEMM_STRASSEN2) {
+    const int64_t mb = M / 4, nb = N / 4;
+    const double t_pre = kernel_time(0, 7.625 * (m * k + k * n), 0, 1, 1.0, P, BW);
+    const double flops = 49.0 / 64.0 * mnk2;
+    // unfused: 49 FP32 products of (M/4 x N/4) written and read back, then C
+    const double t_prod = kernel_time(flops, 6.125 * (m * k + k * n) + 12.25 * m * n,
+                                      49 * cdiv(mb, 128) * cdiv(nb, 128), sms, kEtaLcmaSingle, P, BW);
+    const double t_h = kernel_time(0, 14.25 * m * n, 0, 1, 1.0, P, BW);
+    return t_pre + t_prod + t_h;
   }
   return INFINITY;
 }

@@ -103,11 +103,18 @@ enum {
                                       single-CTA 128x128 Groups, 2 CTA-pair 256x128 Groups           */
 };
 
+/* `device` value of a planning handle (see lcgemm_create). */
+#define LCGEMM_PLANNING_DEVICE (-1)
+
 /*
  * Create a handle bound to CUDA device `device`.  Allocates only a few bytes
  * (the mapped error word); the Strassen workspace grows on first use.
  * Reads environment overrides LCGEMM_PEAK_GFLOPS and LCGEMM_HBM_GBPS.
  * Returns LCGEMM_ERR_ARG for a null `out` or an invalid device.
+ * device = LCGEMM_PLANNING_DEVICE creates a planning handle that makes no CUDA
+ * call at all: it answers lcgemm_select / lcgemm_estimate for a GB300 (152
+ * SMs; LCGEMM_OPT_MAX_CTAS lowers that) and rejects every run with
+ * LCGEMM_ERR_ARG.
  */
 LCGEMM_API int lcgemm_create(lcgemm_t* out, int device);
 
