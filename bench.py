@@ -410,6 +410,10 @@ def run_case(args):
     M, N, K = (dims * 3)[:3] if len(dims) == 1 else dims
     dev = torch.device("cuda", 0)
     h = lcg.Handle(0)
+    if args.plain_kernel:
+        h.set_option(lcg.OPT_PLAIN_KERNEL, args.plain_kernel)
+    if args.lcma_kernel:
+        h.set_option(lcg.OPT_LCMA_KERNEL, args.lcma_kernel)
     A, B = synthetic.operands(M, N, K, "normal", 2, "bf16", str(dev))
     C = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :N]
     for _ in range(args.reps):
@@ -433,6 +437,8 @@ def main():
     ap.add_argument("--case", default=None, help="profiling mode: run one shape 'n' or 'M,N,K' --reps times")
     ap.add_argument("--algo", default="auto", help="algorithm for --case")
     ap.add_argument("--reps", type=int, default=3, help="launches for --case")
+    ap.add_argument("--plain-kernel", type=int, default=0, help="--case: 1 single-CTA, 2 CTA-pair plain kernel")
+    ap.add_argument("--lcma-kernel", type=int, default=0, help="--case: 1 single-CTA, 2 CTA-pair fused kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
