@@ -124,6 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(BF16, kBM, BN);
+      // descriptors of stage 0; a stage / K-step offset is added to the start-address field
+      const uint64_t a_desc0 = sdesc_k128(smem_u32(sA));
+      const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
@@ -139,11 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * C::kABytes) >> 4);
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kBBytes) >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_f16(d_tmem, sdesc_k128(a0 + k * 32), sdesc_k128(b0 + k * 32), idesc, (kb | k) != 0);
+            mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
           mma_commit(&empty[stage]);
           issued = true;
           if (++stage == STAGES) {
