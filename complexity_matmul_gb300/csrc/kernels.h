@@ -84,6 +84,7 @@ struct LcmaArgs {
   int tiles_m, tiles_n, num_groups, group_m;
   LcmaOperand a_src[49], b_src[49];
   float* prod;                    // unfused path: FP32 products [num_products][mb][ldp]
+  float* scratch;                 // CTA-pair fused path: per-CTA FP32 quadrant slots
   int64_t ldp;
   int num_products;
   int* err;
@@ -99,7 +100,9 @@ struct LcmaLaunch {
 };
 cudaError_t launch_lcma_fused(const LcmaLaunch& L, cudaStream_t st);
 cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st);
-// CTA-pair fused one-level kernel: Groups of 256 x 128 quadrant tiles; B maps use 64-row boxes.
+// CTA-pair fused one-level kernel: Groups of 256 x 256 quadrant tiles; A and B maps use 128-row
+// boxes; quadrant sums in a per-CTA FP32 scratch of lcma_pair_scratch_bytes(grid) bytes.
 cudaError_t launch_lcma_pair(const LcmaLaunch& L, cudaStream_t st);
+size_t lcma_pair_scratch_bytes(int grid);
 
 }  // namespace lcg

@@ -1,39 +1,119 @@
-// Fused one-level LCMA kernel on CTA pairs (cta_group::2).
+// Fused one-level LCMA kernel on CTA pairs (cta_group::2) with 256 x 256
+// Group tiles.
 //
-// Same Group program as the single-CTA kernel in lcma_fused.cu (product order
-// M5 M3 M7 M1 M4 M2 M6, four 128-column TMEM buffers, 12 epilogue ops per
-// Group), but a Group covers a 256 x 128 tile of each quadrant: the even CTA
-// of a cluster of two issues tcgen05.mma.cta_group::2 with M = 256, N = 128;
-// each CTA stages 128 rows of the product's A operand and 64 of its 128 B
-// rows, and holds its 128 rows of every buffer in its own tensor memory.
-// Per SM the tensor core then reads 16 KB of A and 8 KB of B per 64-deep K
-// slab for 128 x 128 x 64 MACs (96 B/clk at the tensor peak) instead of
-// 16 KB + 16 KB (128 B/clk) -- the single-CTA 128 x 128 tile is limited by
-// shared-memory bandwidth, the pair tile is not.
+// A Group is the 7 product tiles of one 256 x 256 coordinate of the quadrant
+// grid (FalconGEMM write-up, section "从 LCMA 到 FalconGEMM": the same-position
+// tiles of the 7 batched products run together on one unit and are combined
+// into C there, with no product written to HBM and no atomics).  Each product
+// is one 256 x 256 MMA stream (M = 256 over the pair, N = 256): the same
+// operand footprint per flop as the plain CTA-pair kernel, half the shared-
+// memory traffic of 128-wide product tiles, which is what limits those.
 //
-// Cross-CTA synchronisation:
-//   full[s]       leader's; armed with both CTAs' bytes; both CTAs' copies complete on it
-//   empty[s]      per CTA; the leader's commit arrives on both
-//   mdone[step]   per CTA; the leader's commit arrives on both
-//   progress[4]   per CTA, one counter per epilogue warp; the leader's MMA thread
-//                 reads all eight through distributed shared memory
+// Tensor memory holds two 256-column product accumulators (all 512 columns),
+// so product p+1 accumulates while the epilogue consumes product p.  The four
+// quadrant sums live in FP32 in a per-CTA scratch that stays in L2 (three
+// slots are enough because of the product order):
+//
+//   product  epilogue (P = the product, FP32)           slots after it
+//   M5       s0  = -P ;  s1  = P                         s0=C11 s1=C12
+//   M3       C12 = s1 + P (cast, stored) ;  s1 = P       s1=C22
+//   M7       s0 += P
+//   M1       s0 += P ;  s1 += P
+//   M4       C11 = s0 + P (stored) ;  s2 = P             s2=C21
+//   M2       C21 = s2 + P (stored) ;  s1 -= P
+//   M6       C22 = s1 + P (stored)
+//
+// Every quadrant is accumulated in FP32 and cast once (numerics paragraphs of
+// the write-up's "从缓存重排到 Cost Model" section).  Each epilogue thread owns
+// one accumulator row and 128 columns; the scratch is laid out column-major per
+// slot so that a warp's 32 rows of one column are one 128-byte line.
+//
+// Cross-CTA synchronisation (as in the plain CTA-pair kernel):
+//   full[s]   leader's; armed with both CTAs' bytes; both CTAs' copies complete on it
+//   empty[s]  per CTA; the leader's MMA commit arrives on both
+//   pfull[b]  per CTA; the leader's MMA commit arrives on both when product b is done
+//   pempty[b] leader's; all 16 epilogue warps of the pair arrive when b is consumed
 #include "lcma_program.cuh"
 
 namespace lcg {
 
 namespace {
 
-constexpr int kRows = 128;                 // rows per CTA (256 per pair)
-constexpr int kBN = kBufCols;              // columns per Group tile
+constexpr int kRows = 128;                       // accumulator rows per CTA (256 per pair)
+constexpr int kTileN = 256;                      // Group tile width
 constexpr int kBK = 64;
-constexpr int kStages = 8;
-constexpr int kThreads = 192;
-constexpr int kABytes = kRows * kBK * 2;   // 16 KB
-constexpr int kBBytes = (kBN / 2) * kBK * 2;   // 8 KB
+constexpr int kStages = 6;
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quarter, 128 columns each
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kABytes = kRows * kBK * 2;         // 16 KB
+constexpr int kBBytes = (kTileN / 2) * kBK * 2;  // 16 KB (this CTA's half of B)
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTxBytes = 2 * kStageBytes;
-constexpr int kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 512 + 1024;
+constexpr int kTmemCols = 2 * kTileN;
+constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr int kSlots = 3;
+constexpr int kSlotFloats = kRows * kTileN;      // one slot: 128 rows x 256 columns
+constexpr int kSteps1 = 7;
+
+// Epilogue work per product step: up to two targets.
+enum : int { kTgtNone = 0, kTgtInit = 1, kTgtAcc = 2, kTgtFinal = 3 };
+struct Target {
+  int kind, slot, sign, quad;
+};
+struct StepOps {
+  int product;
+  Target t[2];
+};
+#define LCG_L2_PROGRAM                                                                          \
+  {                                                                                             \
+    {4, {{kTgtInit, 0, -1, 0}, {kTgtInit, 1, 1, 1}}},       /* M5 */                            \
+        {2, {{kTgtFinal, 1, 1, 1}, {kTgtInit, 1, 1, 3}}},   /* M3: C12 done, C22 starts */      \
+        {6, {{kTgtAcc, 0, 1, 0}, {kTgtNone, 0, 0, 0}}},     /* M7 */                            \
+        {0, {{kTgtAcc, 0, 1, 0}, {kTgtAcc, 1, 1, 3}}},      /* M1 */                            \
+        {3, {{kTgtFinal, 0, 1, 0}, {kTgtInit, 2, 1, 2}}},   /* M4: C11 done, C21 starts */      \
+        {1, {{kTgtFinal, 2, 1, 2}, {kTgtAcc, 1, -1, 3}}},   /* M2: C21 done */                  \
+        {5, {{kTgtFinal, 1, 1, 3}, {kTgtNone, 0, 0, 0}}},   /* M6: C22 done */                  \
+  }
+constexpr StepOps kL2Program[kSteps1] = LCG_L2_PROGRAM;
+
+// The program stores every quadrant exactly once with C_q = sum_p W[q,p] M_p.
+struct L2ProgramCheck {
+  bool ok = true;
+  constexpr L2ProgramCheck() {
+    int slot[kSlots][7] = {};
+    int stored[4][7] = {};
+    bool done[4] = {false, false, false, false};
+    for (int s = 0; s < kSteps1; ++s) {
+      const int p = kL2Program[s].product;
+      for (int i = 0; i < 2; ++i) {
+        const Target t = kL2Program[s].t[i];
+        if (t.kind == kTgtInit) {
+          for (int j = 0; j < 7; ++j) slot[t.slot][j] = 0;
+          slot[t.slot][p] = t.sign;
+        } else if (t.kind == kTgtAcc) {
+          slot[t.slot][p] += t.sign;
+        } else if (t.kind == kTgtFinal) {
+          for (int j = 0; j < 7; ++j) stored[t.quad][j] = slot[t.slot][j];
+          stored[t.quad][p] += t.sign;
+          if (done[t.quad]) ok = false;
+          done[t.quad] = true;
+        }
+      }
+      // a Final must read its slot before an Init of the same step overwrites it
+      if (kL2Program[s].t[0].kind == kTgtInit && kL2Program[s].t[1].kind == kTgtFinal &&
+          kL2Program[s].t[0].slot == kL2Program[s].t[1].slot)
+        ok = false;
+    }
+    for (int q = 0; q < 4; ++q) {
+      if (!done[q]) ok = false;
+      for (int j = 0; j < 7; ++j)
+        if (stored[q][j] != kW1[q][j]) ok = false;
+    }
+  }
+};
+static_assert(L2ProgramCheck{}.ok, "the L2-accumulating program must compute C_q = sum_p W[q,p] M_p");
+
+__constant__ StepOps d_l2_program[kSteps1] = LCG_L2_PROGRAM;
 
 __device__ __forceinline__ void load_operand_pair(void* dst, const CUtensorMap* sum_map, const CUtensorMap* raw_map,
                                                   const LcmaOperand& src, uint32_t bar, int k0, int row0) {
@@ -43,41 +123,85 @@ __device__ __forceinline__ void load_operand_pair(void* dst, const CUtensorMap* 
     tma_load_4d_pair(dst, raw_map, bar, k0, src.c, row0, src.r);
 }
 
-// All eight epilogue-warp counters of the pair have reached `target`.
-__device__ __forceinline__ bool pair_counters_reached(uint32_t local0, uint32_t peer0, uint32_t target) {
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    if (ld_acquire_cluster_u32(local0 + 4 * w) < target) return false;
-    if (ld_acquire_cluster_u32(peer0 + 4 * w) < target) return false;
-  }
-  return true;
+__device__ __forceinline__ void tile_coords_l2(int t, const LcmaArgs& a, int& mb, int& nb) {
+  const int group_tiles = a.group_m * a.tiles_n;
+  const int g = t / group_tiles;
+  const int first_m = g * a.group_m;
+  const int rows = min(a.tiles_m - first_m, a.group_m);
+  const int local = t - g * group_tiles;
+  mb = first_m + local % rows;
+  nb = local / rows;
 }
 
-__device__ __forceinline__ bool wait_pair_counters(uint32_t local0, uint32_t peer0, uint32_t target,
-                                                   const WaitCtl& w) {
-  if (pair_counters_reached(local0, peer0, target)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (pair_counters_reached(local0, peer0, target)) return true;
-    if ((i & 31u) == 0) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.timeout_ns) {
-        record_error(w, kErrWaitTimeout);
-        return false;
+// Consume one product held in TMEM (this thread: one row, 128 columns) into
+// the scratch slots / C according to the step's targets.
+// `col0`: first of this thread's 128 columns inside the tile; `tile_col0`: the
+// tile's first column inside the quadrant; `rloc`: this thread's quadrant row.
+template <bool BF16>
+__device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st, float* scratch, int row,
+                                                const LcmaArgs& a, int rloc, int col0, int tile_col0) {
+  uint16_t* Cp = static_cast<uint16_t*>(a.C);
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tsrc + c * 32, r);
+    tmem_wait_ld();
+    const int col = col0 + c * 32;   // column inside the 256-wide tile
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const Target t = st.t[i];
+      if (t.kind == kTgtNone) continue;
+      float* sp = scratch + (static_cast<int64_t>(t.slot) * kTileN + col) * kRows + row;
+      const float sg = static_cast<float>(t.sign);
+      if (t.kind == kTgtInit) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sp[j * kRows] = sg * __uint_as_float(r[j]);
+      } else if (t.kind == kTgtAcc) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sp[j * kRows] = v[j] + sg * __uint_as_float(r[j]);
+      } else {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows] + sg * __uint_as_float(r[j]);
+        // cast once and store into quadrant t.quad of C
+        const int qr = t.quad >> 1, qc = t.quad & 1;
+        uint16_t* crow = Cp + (static_cast<int64_t>(qr) * a.mb + rloc) * a.ldc + static_cast<int64_t>(qc) * a.nb;
+        const int qcol = tile_col0 + col;              // column inside the quadrant
+        if (rloc < a.mb && qcol < a.nb) {
+          const bool vec = (qcol + 32 <= a.nb) && ((reinterpret_cast<uintptr_t>(crow + qcol) & 15u) == 0);
+          if (vec) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + qcol);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 o;
+              o.x = pack2(v[8 * w + 0], v[8 * w + 1], BF16);
+              o.y = pack2(v[8 * w + 2], v[8 * w + 3], BF16);
+              o.z = pack2(v[8 * w + 4], v[8 * w + 5], BF16);
+              o.w = pack2(v[8 * w + 6], v[8 * w + 7], BF16);
+              dst[w] = o;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint32_t p = pack2(v[j], v[j + 1], BF16);
+              if (qcol + j < a.nb) crow[qcol + j] = static_cast<uint16_t>(p & 0xffffu);
+              if (qcol + j + 1 < a.nb) crow[qcol + j + 1] = static_cast<uint16_t>(p >> 16);
+            }
+          }
+        }
       }
     }
   }
 }
 
-__device__ __forceinline__ void red_release_cluster_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.cluster.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    lcma1_pair_kernel(const __grid_constant__ CUtensorMap tmA_sum, const __grid_constant__ CUtensorMap tmA_raw,
-                      const __grid_constant__ CUtensorMap tmB_sum, const __grid_constant__ CUtensorMap tmB_raw,
-                      const LcmaArgs args) {
+    lcma1_l2_kernel(const __grid_constant__ CUtensorMap tmA_sum, const __grid_constant__ CUtensorMap tmA_raw,
+                    const __grid_constant__ CUtensorMap tmB_sum, const __grid_constant__ CUtensorMap tmB_raw,
+                    const LcmaArgs args_in) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem;
@@ -85,11 +209,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* mdone = bars + 2 * kStages;
-  uint64_t* drain = mdone + kSteps;
+  uint64_t* pfull = bars + 2 * kStages;
+  uint64_t* pempty = pfull + 2;
+  uint64_t* drain = pempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  uint32_t* progress = tmem_slot + 1;            // [4]: ops completed per epilogue warp of this CTA
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -101,9 +225,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kSteps; ++s) mbar_init(&mdone[s], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], 2 * kEpiWarps);
+    }
     mbar_init(drain, 1);
-    for (int w = 0; w < 4; ++w) progress[w] = 0;
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA_sum);
@@ -116,8 +242,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
-  const int num_kb = (args.kb + kBK - 1) / kBK;
+  const WaitCtl wc{abort_flag, args_in.err, args_in.timeout_ns};
+  const int num_kb = (args_in.kb + kBK - 1) / kBK;
   const int pair = blockIdx.x / 2;
   const int num_pairs = gridDim.x / 2;
 
@@ -126,11 +252,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int t = pair; ok && t < args.num_groups; t += num_pairs) {
+      for (int t = pair; ok && t < args_in.num_groups; t += num_pairs) {
         int mb, nb;
-        tile_coords(t, args, mb, nb);
-        for (int s = 0; ok && s < kSteps; ++s) {
-          const int p = d_step_product[s];
+        tile_coords_l2(t, args_in, mb, nb);
+        for (int s = 0; ok && s < kSteps1; ++s) {
+          const int p = d_l2_program[s].product;
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
               ok = false;
@@ -138,10 +264,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (leader) mbar_arrive_expect_tx(&full[stage], kTxBytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-            load_operand_pair(sA + stage * kABytes, &tmA_sum, &tmA_raw, args.a_src[p], bar, kb * kBK,
+            load_operand_pair(sA + stage * kABytes, &tmA_sum, &tmA_raw, args_in.a_src[p], bar, kb * kBK,
                               mb * 2 * kRows + static_cast<int>(rank) * kRows);
-            load_operand_pair(sB + stage * kBBytes, &tmB_sum, &tmB_raw, args.b_src[p], bar, kb * kBK,
-                              nb * kBN + static_cast<int>(rank) * (kBN / 2));
+            load_operand_pair(sB + stage * kBBytes, &tmB_sum, &tmB_raw, args_in.b_src[p], bar, kb * kBK,
+                              nb * kTileN + static_cast<int>(rank) * (kTileN / 2));
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
@@ -162,23 +288,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_f16(BF16, 2 * kRows, kBN);
-      // descriptors of stage 0; a stage / K-step offset is added to the start-address field
+      constexpr uint32_t idesc = idesc_f16(BF16, 2 * kRows, kTileN);
       const uint64_t a_desc0 = sdesc_k128(smem_u32(sA));
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
-      const uint32_t ctr_local = mapa_shared(smem_u32(progress), 0);
-      const uint32_t ctr_peer = mapa_shared(smem_u32(progress), 1);
-      uint32_t stage = 0, phase = 0, g = 0;
+      uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
       bool ok = true, issued = false;
-      for (int t = pair; ok && t < args.num_groups; t += num_pairs, ++g) {
-        for (int s = 0; ok && s < kSteps; ++s) {
-          const int need = static_cast<int>(g) * kNumOps + d_step_need[s];
-          if (need > 0 && !wait_pair_counters(ctr_local, ctr_peer, static_cast<uint32_t>(need), wc)) {
+      for (int t = pair; ok && t < args_in.num_groups; t += num_pairs) {
+        for (int s = 0; ok && s < kSteps1; ++s) {
+          if (!mbar_wait(&pempty[buf], buf_phase ^ 1, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + d_step_buf[s] * kBN;
+          const uint32_t d_tmem = tmem_base + buf * kTileN;
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait(&full[stage], phase, wc)) {
               ok = false;
@@ -188,9 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
             const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc,
-                           (d_step_fresh[s] && kb == 0 && k == 0) ? 0u : 1u);
+            for (int k = 0; k < kBK / 16; ++k) mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
             mma_commit_pair(&empty[stage]);
             issued = true;
             if (++stage == kStages) {
@@ -198,7 +318,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               phase ^= 1;
             }
           }
-          if (ok && d_step_has_ops[s]) mma_commit_pair(&mdone[s]);
+          if (!ok) break;
+          mma_commit_pair(&pfull[buf]);
+          buf ^= 1;
+          if (buf == 0) buf_phase ^= 1;
         }
       }
       if (!ok && issued) {
@@ -208,33 +331,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t g = 0;
+    // ------------------------------------------------------------ epilogue (both CTAs, 8 warps)
+    const int ew = warp - 2;
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int half = ew >> 2;               // which 128 of the 256 columns
+    const int row = q * 32 + lane;          // accumulator row inside this CTA's 128
+    float* scratch = args_in.scratch + static_cast<int64_t>(blockIdx.x) * kSlots * kSlotFloats;
+    uint32_t buf = 0, buf_phase = 0;
     bool ok = true;
-    for (int t = pair; ok && t < args.num_groups; t += num_pairs, ++g) {
+    for (int t = pair; ok && t < args_in.num_groups; t += num_pairs) {
       int mb, nb;
-      tile_coords(t, args, mb, nb);
-      const int rloc = mb * 2 * kRows + static_cast<int>(rank) * kRows + q * 32 + lane;
-      int waited = -1;
-      for (int i = 0; i < kNumOps; ++i) {
-        const Op o = d_ops[i];
-        if (o.after != waited) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&mdone[o.after], g & 1u, wc));
-          if (!ok) break;
-          tc_fence_after();
-          waited = o.after;
-        }
-        if (o.kind == kOpStore) {
-          store_quadrant<BF16>(lane_base + o.src * kBN, args, o.quad, rloc, nb * kBN);
-        } else {
-          combine_buffers(lane_base + o.dst * kBN, lane_base + o.src * kBN, static_cast<float>(o.sign),
-                          o.kind == kOpAdd);
-        }
+      tile_coords_l2(t, args_in, mb, nb);
+      const int rloc = mb * 2 * kRows + static_cast<int>(rank) * kRows + row;   // row inside the quadrant
+      for (int s = 0; s < kSteps1; ++s) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&pfull[buf], buf_phase, wc));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tsrc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + half * 128;
+        consume_product<BF16>(tsrc, d_l2_program[s], scratch, row, args_in, rloc, half * 128, nb * kTileN);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) red_release_cluster_add(progress + q, 1u);
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&pempty[buf]), 0));
+        buf ^= 1;
+        if (buf == 0) buf_phase ^= 1;
       }
     }
   }
@@ -249,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <bool BF16>
 cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
-  auto kern = lcma1_pair_kernel<BF16>;
+  auto kern = lcma1_l2_kernel<BF16>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -262,8 +381,10 @@ cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
 
 }  // namespace
 
+size_t lcma_pair_scratch_bytes(int grid) { return static_cast<size_t>(grid) * kSlots * kSlotFloats * sizeof(float); }
+
 cudaError_t launch_lcma_pair(const LcmaLaunch& L, cudaStream_t st) {
-  if (L.levels != 1 || L.grid % 2) return cudaErrorInvalidValue;
+  if (L.levels != 1 || L.grid % 2 || !L.args.scratch) return cudaErrorInvalidValue;
   return L.bf16 ? launch_impl<true>(L, st) : launch_impl<false>(L, st);
 }
 

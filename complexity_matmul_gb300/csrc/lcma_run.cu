@@ -42,11 +42,13 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   const int64_t b_bytes = round_up(nbs * nb * kb * 2, 256);
   const int64_t ldp = round_up(nb, 4);
   const int64_t p_bytes = fused ? 0 : round_up(int64_t(plan.R) * mb * ldp * 4, 256);
-  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes), st);
+  const int64_t s_bytes = fused ? round_up(static_cast<int64_t>(lcma_pair_scratch_bytes(grid_cap(h))), 256) : 0;
+  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes + s_bytes), st);
   if (rc) return rc;
   uint16_t* wsA = static_cast<uint16_t*>(h->ws);
   uint16_t* wsB = reinterpret_cast<uint16_t*>(static_cast<char*>(h->ws) + a_bytes);
   float* prod = reinterpret_cast<float*>(static_cast<char*>(h->ws) + a_bytes + b_bytes);
+  float* scratch = reinterpret_cast<float*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes);
 
   // ---- Combine-A/B pre-pass
   CombineArgs ca{};
@@ -55,10 +57,10 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   if (launch_combine_ab(ca, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
 
   // ---- products
-  // fused one-level Groups run on CTA pairs (256 x 128 tiles) unless the quadrant is small
+  // fused one-level Groups run on CTA pairs (256 x 256 tiles) unless the quadrant is small
   const bool pair = fused && L == 1 && grid_cap(h) >= 2 &&
                     (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
-  const int b_box = pair ? 64 : 128;
+  const int b_box = 128;
   LcmaLaunch ll{};
   ll.levels = L;
   ll.bf16 = bf16;
@@ -87,9 +89,9 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   a.nb = static_cast<int>(nb);
   a.kb = static_cast<int>(kb);
   a.tiles_m = static_cast<int>(pair ? (mb + 255) / 256 : (mb + 127) / 128);
-  a.tiles_n = static_cast<int>((nb + 127) / 128);
+  a.tiles_n = static_cast<int>(pair ? (nb + 255) / 256 : (nb + 127) / 128);
   a.num_groups = a.tiles_m * a.tiles_n;
-  a.group_m = 16;
+  a.group_m = pair ? 8 : 12;   // ~square wave footprint: sqrt(#pairs) resp. sqrt(#CTAs) tile rows
   for (int p = 0; p < plan.R; ++p) {
     // A is stored by (block row, block column); B (K x N stored N x K) by (N block, K block)
     const auto& sa = plan.side[0];
@@ -98,6 +100,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
     a.b_src[p] = sb.slot[p] >= 0 ? LcmaOperand{sb.slot[p], 0, 0} : LcmaOperand{-1, sb.alias_c[p], sb.alias_r[p]};
   }
   a.prod = prod;
+  a.scratch = scratch;
   a.ldp = ldp;
   a.num_products = plan.R;
   a.err = h->err_dev;
