@@ -85,6 +85,10 @@ struct LcmaArgs {
   LcmaOperand a_src[49], b_src[49];
   float* prod;                    // unfused path: FP32 products [num_products][mb][ldp]
   float* scratch;                 // CTA-pair fused path: per-CTA FP32 quadrant slots
+  int num_items;                  // CTA-pair fused path: work items (whole Groups + split halves)
+  int split_first;                // items >= split_first are halves of split tail Groups
+  int* flags;                     // one counter per split Group and CTA rank (zeroed before launch)
+  int debug_drop;                 // test hook: second halves never publish
   int64_t ldp;
   int num_products;
   int* err;

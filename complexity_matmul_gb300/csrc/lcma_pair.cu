@@ -55,8 +55,9 @@ constexpr int kSlots = 3;
 constexpr int kSlotFloats = kRows * kTileN;      // one slot: 128 rows x 256 columns
 constexpr int kSteps1 = 7;
 
-// Epilogue work per product step: up to two targets.
-enum : int { kTgtNone = 0, kTgtInit = 1, kTgtAcc = 2, kTgtFinal = 3 };
+// Epilogue work per product step: up to two targets.  kTgtFinalX adds the
+// partner half's partial sum (split Groups) before the cast.
+enum : int { kTgtNone = 0, kTgtInit = 1, kTgtAcc = 2, kTgtFinal = 3, kTgtFinalX = 4 };
 struct Target {
   int kind, slot, sign, quad;
 };
@@ -64,56 +65,140 @@ struct StepOps {
   int product;
   Target t[2];
 };
-#define LCG_L2_PROGRAM                                                                          \
-  {                                                                                             \
-    {4, {{kTgtInit, 0, -1, 0}, {kTgtInit, 1, 1, 1}}},       /* M5 */                            \
-        {2, {{kTgtFinal, 1, 1, 1}, {kTgtInit, 1, 1, 3}}},   /* M3: C12 done, C22 starts */      \
-        {6, {{kTgtAcc, 0, 1, 0}, {kTgtNone, 0, 0, 0}}},     /* M7 */                            \
-        {0, {{kTgtAcc, 0, 1, 0}, {kTgtAcc, 1, 1, 3}}},      /* M1 */                            \
-        {3, {{kTgtFinal, 0, 1, 0}, {kTgtInit, 2, 1, 2}}},   /* M4: C11 done, C21 starts */      \
-        {1, {{kTgtFinal, 2, 1, 2}, {kTgtAcc, 1, -1, 3}}},   /* M2: C21 done */                  \
-        {5, {{kTgtFinal, 1, 1, 3}, {kTgtNone, 0, 0, 0}}},   /* M6: C22 done */                  \
-  }
-constexpr StepOps kL2Program[kSteps1] = LCG_L2_PROGRAM;
 
-// The program stores every quadrant exactly once with C_q = sum_p W[q,p] M_p.
+// Work item types: a whole Group, or one of the two halves of a split Group
+// (FalconGEMM write-up, "从 LCMA 到 FalconGEMM": a Group may be split over two
+// units; scheduling stays per Group, execution per tile).
+enum : int { kItemFull = 0, kItemFirst = 1, kItemSecond = 2 };
+constexpr int kItemSteps[3] = {7, 4, 3};
+
+#define LCG_L2_PROGRAMS                                                                                      \
+  {                                                                                                          \
+    {/* whole Group */                                                                                       \
+     {4, {{kTgtInit, 0, -1, 0}, {kTgtInit, 1, 1, 1}}},     /* M5: s0 = -M5 (C11), s1 = M5 (C12) */          \
+     {2, {{kTgtFinal, 1, 1, 1}, {kTgtInit, 1, 1, 3}}},     /* M3: C12 = s1 + M3; s1 = M3 (C22) */           \
+     {6, {{kTgtAcc, 0, 1, 0}, {kTgtNone, 0, 0, 0}}},       /* M7: s0 += M7 */                               \
+     {0, {{kTgtAcc, 0, 1, 0}, {kTgtAcc, 1, 1, 3}}},        /* M1: s0 += M1, s1 += M1 */                     \
+     {3, {{kTgtFinal, 0, 1, 0}, {kTgtInit, 2, 1, 2}}},     /* M4: C11 = s0 + M4; s2 = M4 (C21) */           \
+     {1, {{kTgtFinal, 2, 1, 2}, {kTgtAcc, 1, -1, 3}}},     /* M2: C21 = s2 + M2; s1 -= M2 */                \
+     {5, {{kTgtFinal, 1, 1, 3}, {kTgtNone, 0, 0, 0}}}},    /* M6: C22 = s1 + M6 */                          \
+    {/* first half: M5 M3 M7 M1; finishes C11 and C22 with the second half's partials */                    \
+     {4, {{kTgtInit, 0, -1, 0}, {kTgtInit, 1, 1, 1}}},                                                       \
+     {2, {{kTgtFinal, 1, 1, 1}, {kTgtInit, 1, 1, 3}}},                                                       \
+     {6, {{kTgtAcc, 0, 1, 0}, {kTgtNone, 0, 0, 0}}},                                                         \
+     {0, {{kTgtFinalX, 0, 1, 0}, {kTgtFinalX, 1, 1, 3}}},  /* C11 = s0 + M1 + p0, C22 = s1 + M1 + p1 */      \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}}},                                                       \
+    {/* second half: M4 M2 M6; finishes C21, publishes p0 = M4 (C11) and p1 = M6 - M2 (C22) */               \
+     {3, {{kTgtInit, 0, 1, 0}, {kTgtInit, 2, 1, 2}}},                                                        \
+     {1, {{kTgtFinal, 2, 1, 2}, {kTgtInit, 1, -1, 3}}},                                                      \
+     {5, {{kTgtAcc, 1, 1, 3}, {kTgtNone, 0, 0, 0}}},                                                         \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
+     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}}},                                                       \
+  }
+constexpr StepOps kL2Programs[3][kSteps1] = LCG_L2_PROGRAMS;
+
+// Every item type stores each of its quadrants once; together the two halves
+// of a split Group produce exactly C_q = sum_p W[q,p] M_p for all four.
 struct L2ProgramCheck {
   bool ok = true;
-  constexpr L2ProgramCheck() {
-    int slot[kSlots][7] = {};
-    int stored[4][7] = {};
-    bool done[4] = {false, false, false, false};
-    for (int s = 0; s < kSteps1; ++s) {
-      const int p = kL2Program[s].product;
+  constexpr void run(int type, int (&slot)[kSlots][7], int (&stored)[4][7], bool (&done)[4],
+                     const int (&partner)[kSlots][7]) {
+    for (int s = 0; s < kItemSteps[type]; ++s) {
+      const int p = kL2Programs[type][s].product;
       for (int i = 0; i < 2; ++i) {
-        const Target t = kL2Program[s].t[i];
+        const Target t = kL2Programs[type][s].t[i];
         if (t.kind == kTgtInit) {
           for (int j = 0; j < 7; ++j) slot[t.slot][j] = 0;
           slot[t.slot][p] = t.sign;
         } else if (t.kind == kTgtAcc) {
           slot[t.slot][p] += t.sign;
-        } else if (t.kind == kTgtFinal) {
-          for (int j = 0; j < 7; ++j) stored[t.quad][j] = slot[t.slot][j];
+        } else if (t.kind == kTgtFinal || t.kind == kTgtFinalX) {
+          for (int j = 0; j < 7; ++j)
+            stored[t.quad][j] = slot[t.slot][j] + (t.kind == kTgtFinalX ? partner[t.slot][j] : 0);
           stored[t.quad][p] += t.sign;
           if (done[t.quad]) ok = false;
           done[t.quad] = true;
         }
       }
-      // a Final must read its slot before an Init of the same step overwrites it
-      if (kL2Program[s].t[0].kind == kTgtInit && kL2Program[s].t[1].kind == kTgtFinal &&
-          kL2Program[s].t[0].slot == kL2Program[s].t[1].slot)
+      if (kL2Programs[type][s].t[0].kind == kTgtInit && kL2Programs[type][s].t[1].kind >= kTgtFinal &&
+          kL2Programs[type][s].t[0].slot == kL2Programs[type][s].t[1].slot)
         ok = false;
     }
-    for (int q = 0; q < 4; ++q) {
-      if (!done[q]) ok = false;
-      for (int j = 0; j < 7; ++j)
-        if (stored[q][j] != kW1[q][j]) ok = false;
+  }
+  constexpr L2ProgramCheck() {
+    const int none[kSlots][7] = {};
+    {
+      int slot[kSlots][7] = {};
+      int stored[4][7] = {};
+      bool done[4] = {false, false, false, false};
+      run(kItemFull, slot, stored, done, none);
+      for (int q = 0; q < 4; ++q) {
+        if (!done[q]) ok = false;
+        for (int j = 0; j < 7; ++j)
+          if (stored[q][j] != kW1[q][j]) ok = false;
+      }
+    }
+    {
+      int slot2[kSlots][7] = {};
+      int stored[4][7] = {};
+      bool done[4] = {false, false, false, false};
+      run(kItemSecond, slot2, stored, done, none);      // publishes slot2[0], slot2[1]
+      int slot1[kSlots][7] = {};
+      run(kItemFirst, slot1, stored, done, slot2);
+      for (int q = 0; q < 4; ++q) {
+        if (!done[q]) ok = false;
+        for (int j = 0; j < 7; ++j)
+          if (stored[q][j] != kW1[q][j]) ok = false;
+      }
     }
   }
 };
-static_assert(L2ProgramCheck{}.ok, "the L2-accumulating program must compute C_q = sum_p W[q,p] M_p");
+static_assert(L2ProgramCheck{}.ok, "the L2-accumulating programs must compute C_q = sum_p W[q,p] M_p");
 
-__constant__ StepOps d_l2_program[kSteps1] = LCG_L2_PROGRAM;
+__constant__ StepOps d_l2_programs[3][kSteps1] = LCG_L2_PROGRAMS;
+__constant__ int d_item_steps[3] = {7, 4, 3};
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for a split Group's partner: *flag >= target, else kErrFixupTimeout.
+__device__ __forceinline__ bool wait_flag(const int* flag, int target, const WaitCtl& w) {
+  if (ld_acquire_gpu(flag) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    if ((i & 31u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        record_error(w, kErrFixupTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Work item w of this launch -> Group index and item type.
+__device__ __forceinline__ void item_of(int w, const LcmaArgs& a, int& group, int& type) {
+  if (w < a.split_first) {
+    group = w;
+    type = kItemFull;
+  } else {
+    const int i = (w - a.split_first) >> 1;
+    group = a.split_first + i;
+    type = ((w - a.split_first) & 1) ? kItemSecond : kItemFirst;
+  }
+}
 
 __device__ __forceinline__ void load_operand_pair(void* dst, const CUtensorMap* sum_map, const CUtensorMap* raw_map,
                                                   const LcmaOperand& src, uint32_t bar, int k0, int row0) {
@@ -139,7 +224,8 @@ __device__ __forceinline__ void tile_coords_l2(int t, const LcmaArgs& a, int& mb
 // tile's first column inside the quadrant; `rloc`: this thread's quadrant row.
 template <bool BF16>
 __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st, float* scratch, int row,
-                                                const LcmaArgs& a, int rloc, int col0, int tile_col0) {
+                                                const LcmaArgs& a, int rloc, int col0, int tile_col0,
+                                                const float* partner) {
   uint16_t* Cp = static_cast<uint16_t*>(a.C);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
@@ -166,6 +252,11 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows] + sg * __uint_as_float(r[j]);
+        if (t.kind == kTgtFinalX) {
+          const float* pp = partner + (static_cast<int64_t>(t.slot) * kTileN + col) * kRows + row;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += __ldcg(pp + j * kRows);
+        }
         // cast once and store into quadrant t.quad of C
         const int qr = t.quad >> 1, qc = t.quad & 1;
         uint16_t* crow = Cp + (static_cast<int64_t>(qr) * a.mb + rloc) * a.ldc + static_cast<int64_t>(qc) * a.nb;
@@ -252,11 +343,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int t = pair; ok && t < args_in.num_groups; t += num_pairs) {
+      for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
+        int grp, type;
+        item_of(w, args_in, grp, type);
         int mb, nb;
-        tile_coords_l2(t, args_in, mb, nb);
-        for (int s = 0; ok && s < kSteps1; ++s) {
-          const int p = d_l2_program[s].product;
+        tile_coords_l2(grp, args_in, mb, nb);
+        const int nsteps = d_item_steps[type];
+        for (int s = 0; ok && s < nsteps; ++s) {
+          const int p = d_l2_programs[type][s].product;
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
               ok = false;
@@ -293,8 +387,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
       uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
       bool ok = true, issued = false;
-      for (int t = pair; ok && t < args_in.num_groups; t += num_pairs) {
-        for (int s = 0; ok && s < kSteps1; ++s) {
+      for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
+        int grp, type;
+        item_of(w, args_in, grp, type);
+        const int nsteps = d_item_steps[type];
+        for (int s = 0; ok && s < nsteps; ++s) {
           if (!mbar_wait(&pempty[buf], buf_phase ^ 1, wc)) {
             ok = false;
             break;
@@ -339,21 +436,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float* scratch = args_in.scratch + static_cast<int64_t>(blockIdx.x) * kSlots * kSlotFloats;
     uint32_t buf = 0, buf_phase = 0;
     bool ok = true;
-    for (int t = pair; ok && t < args_in.num_groups; t += num_pairs) {
+    for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
+      int grp, type;
+      item_of(w, args_in, grp, type);
       int mb, nb;
-      tile_coords_l2(t, args_in, mb, nb);
+      tile_coords_l2(grp, args_in, mb, nb);
       const int rloc = mb * 2 * kRows + static_cast<int>(rank) * kRows + row;   // row inside the quadrant
-      for (int s = 0; s < kSteps1; ++s) {
+      const int nsteps = d_item_steps[type];
+      // split Groups: the halves meet through the second half's scratch and a counter
+      const int split_idx = (w - args_in.split_first) >> 1;
+      int* flag = type == kItemFull ? nullptr : args_in.flags + 2 * split_idx + static_cast<int>(rank);
+      const float* partner = nullptr;
+      if (type == kItemFirst) {
+        const int partner_pair = (args_in.split_first + 2 * split_idx + 1) % num_pairs;
+        partner = args_in.scratch + static_cast<int64_t>(2 * partner_pair + static_cast<int>(rank)) * kSlots * kSlotFloats;
+      }
+      for (int s = 0; s < nsteps; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(&pfull[buf], buf_phase, wc));
         if (!ok) break;
         tc_fence_after();
+        if (type == kItemFirst && s == nsteps - 1) {
+          // all 8 epilogue warps of the partner CTA with this rank have published (bounded wait)
+          ok = __all_sync(0xffffffffu, wait_flag(flag, kEpiWarps, wc));
+          if (!ok) break;
+        }
         const uint32_t tsrc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + half * 128;
-        consume_product<BF16>(tsrc, d_l2_program[s], scratch, row, args_in, rloc, half * 128, nb * kTileN);
+        consume_product<BF16>(tsrc, d_l2_programs[type][s], scratch, row, args_in, rloc, half * 128, nb * kTileN,
+                              partner);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&pempty[buf]), 0));
         buf ^= 1;
         if (buf == 0) buf_phase ^= 1;
+      }
+      if (ok && type == kItemSecond) {
+        // publish this warp's partial sums (slots 0 and 1) to the first half
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && !args_in.debug_drop) red_release_gpu_add(flag, 1);
       }
     }
   }

@@ -43,7 +43,8 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   const int64_t ldp = round_up(nb, 4);
   const int64_t p_bytes = fused ? 0 : round_up(int64_t(plan.R) * mb * ldp * 4, 256);
   const int64_t s_bytes = fused ? round_up(static_cast<int64_t>(lcma_pair_scratch_bytes(grid_cap(h))), 256) : 0;
-  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes + s_bytes), st);
+  const int64_t f_bytes = fused ? round_up(int64_t(sizeof(int)) * grid_cap(h), 256) : 0;   // split flags
+  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes + s_bytes + f_bytes), st);
   if (rc) return rc;
   uint16_t* wsA = static_cast<uint16_t*>(h->ws);
   uint16_t* wsB = reinterpret_cast<uint16_t*>(static_cast<char*>(h->ws) + a_bytes);
@@ -106,7 +107,17 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
   if (pair) {
-    ll.grid = 2 * std::min(a.num_groups, grid_cap(h) / 2);
+    // Stream-K style split of the tail: when the last, partial wave of Groups
+    // fits twice over, its Groups run as two halves on two pairs each.
+    const int P = grid_cap(h) / 2;
+    const int full_waves = a.num_groups / P, rem = a.num_groups - full_waves * P;
+    const bool split = h->split && rem > 0 && 2 * rem <= P;
+    a.split_first = split ? full_waves * P : a.num_groups;
+    a.num_items = split ? full_waves * P + 2 * rem : a.num_groups;
+    a.flags = split ? reinterpret_cast<int*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes + s_bytes) : nullptr;
+    a.debug_drop = h->debug_drop;
+    if (split && cudaMemsetAsync(a.flags, 0, sizeof(int) * 2 * rem, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    ll.grid = 2 * std::min(a.num_items, P);
     if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     return LCGEMM_OK;
   }

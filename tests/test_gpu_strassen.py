@@ -197,3 +197,54 @@ def test_repeated_and_interleaved_launches(h):
     assert h.sync_status() == 0
     for i, C in outs[-len(shapes) * len(STRASSEN):]:
         assert_bit_exact(C, refs[i], "f16")
+
+
+# ---------------------------------------------------------------- Stream-K split of tail Groups (CTA-pair kernel)
+
+@pytest.fixture(scope="module")
+def hp():
+    handle = lcg.Handle(0)
+    handle.set_option(lcg.OPT_LCMA_KERNEL, 2)
+    yield handle
+    handle.close()
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 1024), (1536, 2560, 512), (8704, 8704, 256), (512, 768, 1024)])
+def test_split_on_off_integer_bit_exact(hp, M, N, K):
+    """Split tail Groups (two halves on two CTA pairs, fixed up through L2) give the exact result."""
+    A, B = synthetic.operands(M, N, K, "int3", 12, "bf16", "cuda")
+    rows = None if M * N <= 4096 * 4096 else synthetic.row_sample(M, 128)
+    ref = oracle_c64(A, B, "bf16", rows=rows)
+    for split in (1, 0):
+        hp.set_option(lcg.OPT_SPLIT, split)
+        C = _run(hp, A, B, "strassen1")
+        assert_bit_exact(C, ref, "bf16", rows=rows)
+    hp.set_option(lcg.OPT_SPLIT, 1)
+
+
+def test_split_float_tolerance(hp):
+    A, B = synthetic.operands(2048, 2048, 2048, "normal", 13, "bf16", "cuda")
+    ref = oracle_c64(A, B, "bf16")
+    hp.set_option(lcg.OPT_SPLIT, 1)
+    assert_close(_run(hp, A, B, "strassen1"), ref, "bf16", "strassen1")
+
+
+def test_partner_signal_timeout_is_reported_and_recovered():
+    """Failure detection without a GPU fault: the second halves of split Groups never publish,
+    so the first halves' bounded waits run out; the kernel ends, the next status call reports
+    LCGEMM_ERR_TIMEOUT, and the handle keeps working."""
+    h2 = lcg.Handle(0)
+    h2.set_option(lcg.OPT_LCMA_KERNEL, 2)
+    h2.set_option(lcg.OPT_WAIT_TIMEOUT_US, 50000)
+    A, B = synthetic.operands(2048, 2048, 1024, "int3", 14, "bf16", "cuda")
+    h2.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 1)
+    h2.run(A, B, algo="strassen1")
+    torch.cuda.synchronize()
+    assert h2.sync_status() == lcg.ERR_TIMEOUT
+    assert h2.sync_status() == lcg.OK          # reported once, then cleared
+    h2.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 0)
+    C = h2.run(A, B, algo="strassen1")
+    torch.cuda.synchronize()
+    assert h2.sync_status() == lcg.OK
+    assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
+    h2.close()
