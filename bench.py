@@ -426,6 +426,87 @@ def run_case(args):
         sys.exit(1)
 
 
+def _time_launch(h, A, B, C, algo, reps, flush):
+    """Median device time (s) of `reps` launches, L2 flushed before each."""
+    import torch
+    for _ in range(2):
+        h.run(A, B, C, algo=algo)
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        h.run(A, B, C, algo=algo)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def run_grid(args):
+    """Cost-model accuracy on the FP16 shape grid: time every eligible algorithm per
+    (M, N, K), check that `auto`'s choice is within 2 % of the fastest one."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    triples = synthetic.grid_quick_subset() if args.grid == "quick" else synthetic.grid_triples()
+    dev = torch.device("cuda", 0)
+    h = lcg.Handle(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    rows, correct = [], 0
+    for (M, N, K) in triples:
+        A = synthetic.matrix(M, K, "normal", 1003, "f16", str(dev), scale=1.0 / K ** 0.5)
+        B = synthetic.matrix(N, K, "normal", 2003, "f16", str(dev))
+        C = torch.empty((M, N), dtype=torch.float16, device=dev)
+        times = {}
+        for algo in ("plain", "strassen1", "strassen2"):
+            try:
+                h.estimate(M, N, K, lcg.F16, algo)
+            except lcg.LcgemmError:
+                continue
+            times[algo] = _time_launch(h, A, B, C, algo, args.grid_reps, flush)
+        chosen = lcg.ALGO_NAMES[h.select(M, N, K, lcg.F16)]
+        best = min(times, key=times.get)
+        ok = times[chosen] <= 1.02 * times[best]
+        correct += ok
+        rows.append({"M": M, "N": N, "K": K, "chosen": chosen, "best": best, "ok": bool(ok),
+                     "tflops": {a: round(2.0 * M * N * K / t / 1e12, 2) for a, t in times.items()},
+                     "pred_ms": {a: round(h.estimate(M, N, K, lcg.F16, a) * 1e3, 4) for a in times},
+                     "ms": {a: round(t * 1e3, 4) for a, t in times.items()}})
+        del A, B, C
+    rc = h.sync_status()
+    summary = {"grid": args.grid, "shapes": len(triples), "auto_within_2pct": correct,
+               "fraction": round(correct / len(triples), 4), "status": rc,
+               "fastest_counts": {a: sum(r["best"] == a for r in rows) for a in ("plain", "strassen1", "strassen2")}}
+    print(json.dumps(summary), flush=True)
+    if args.grid_out:
+        with open(args.grid_out, "w") as f:
+            json.dump({"summary": summary, "rows": rows}, f)
+
+
+def run_skinny(args):
+    """LLM-shaped skinny BF16 GEMMs: time per shape, effective TFLOPS and HBM GB/s."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    dev = torch.device("cuda", 0)
+    h = lcg.Handle(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    _, _, hbm, kind = _peaks()
+    for (M, N, K) in synthetic.SKINNY:
+        A = synthetic.matrix(M, K, "normal", 1004, "bf16", str(dev))
+        B = synthetic.matrix(N, K, "normal", 2004, "bf16", str(dev), scale=0.02)
+        C = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :N]
+        t = _time_launch(h, A, B, C, "auto", args.grid_reps, flush)
+        byts = 2.0 * (M * K + K * N + M * N)
+        print(json.dumps({"M": M, "N": N, "K": K, "us": round(t * 1e6, 2), "tflops": round(2.0 * M * N * K / t / 1e12, 2),
+                          "GBps": round(byts / t / 1e9, 1), "hbm_frac": round(byts / t / 1e9 / hbm, 3),
+                          "algo": lcg.ALGO_NAMES[h.last_algo()]}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,11 +520,20 @@ def main():
     ap.add_argument("--reps", type=int, default=3, help="launches for --case")
     ap.add_argument("--plain-kernel", type=int, default=0, help="--case: 1 single-CTA, 2 CTA-pair plain kernel")
     ap.add_argument("--lcma-kernel", type=int, default=0, help="--case: 1 single-CTA, 2 CTA-pair fused kernel")
+    ap.add_argument("--grid", choices=["quick", "full"], default=None,
+                    help="cost-model accuracy on the FP16 shape grid (100-triple subset or all 1000)")
+    ap.add_argument("--grid-out", default=None, help="--grid: write per-shape results to this JSON file")
+    ap.add_argument("--grid-reps", type=int, default=5, help="--grid/--skinny: timed launches per algorithm")
+    ap.add_argument("--skinny", action="store_true", help="time the LLM-shaped skinny GEMMs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.case:
         run_case(args)
+    elif args.grid:
+        run_grid(args)
+    elif args.skinny:
+        run_skinny(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

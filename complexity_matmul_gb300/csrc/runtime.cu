@@ -41,7 +41,7 @@ namespace {
 // bandwidth the streaming kernels reach.  Measured on GB300 (1 CTA per SM).
 constexpr double kEtaPlainPair = 0.86;    // CTA-pair 256 x 256 tiles
 constexpr double kEtaPlainSingle = 0.78;  // single-CTA 128 x 256 tiles
-constexpr double kEtaLcmaPair = 0.80;     // fused one-level Groups on CTA pairs (256 x 128, 7 products)
+constexpr double kEtaLcmaPair = 0.70;     // fused one-level Groups on CTA pairs (256 x 256, 7 products)
 constexpr double kEtaLcmaSingle = 0.55;   // single-CTA 128 x 128 product tiles (shared-memory bound)
 constexpr double kBetaStream = 0.80;      // combine pre-pass / recombination, fraction of HBM bandwidth
 constexpr double kLaunchSec = 6e-6;       // launch + prologue + pipeline fill of one kernel
@@ -50,6 +50,15 @@ double wave_efficiency(int64_t tiles, int units) {
   if (tiles <= 0 || units <= 0) return 1.0;
   const int64_t waves = (tiles + units - 1) / units;
   return static_cast<double>(tiles) / static_cast<double>(waves * units);
+}
+
+// Same with the tail split: when the partial last wave fits twice over, its
+// Groups run as halves (the longer half is 4 of 7 products).
+double wave_efficiency_split(int64_t tiles, int units) {
+  if (tiles <= 0 || units <= 0) return 1.0;
+  const int64_t full = tiles / units, rem = tiles - full * units;
+  const double waves = static_cast<double>(full) + (rem == 0 ? 0.0 : (2 * rem <= units ? 4.0 / 7.0 : 1.0));
+  return static_cast<double>(tiles) / (waves * units);
 }
 
 // One kernel on the roofline: compute time at eta * peak stretched by wave
@@ -86,9 +95,13 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
     if (algo == LCGEMM_STRASSEN1) {
       const double bytes = 3.5 * (m * k + k * n) + 2.0 * m * n;
       const bool pair = sms >= 2 && (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
-      const double t = pair ? kernel_time(flops, bytes, cdiv(mb, 256) * cdiv(nb, 128), sms / 2, kEtaLcmaPair, P, BW)
-                            : kernel_time(flops, bytes, cdiv(mb, 128) * cdiv(nb, 128), sms, kEtaLcmaSingle, P, BW);
-      return t_pre + t;
+      if (pair) {
+        const int64_t groups = cdiv(mb, 256) * cdiv(nb, 256);
+        const double eff = h->split ? wave_efficiency_split(groups, sms / 2) : wave_efficiency(groups, sms / 2);
+        const double t = std::max(flops / (kEtaLcmaPair * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
+        return t_pre + t;
+      }
+      return t_pre + kernel_time(flops, bytes, cdiv(mb, 128) * cdiv(nb, 128), sms, kEtaLcmaSingle, P, BW);
     }
     const double t_prod = kernel_time(flops, 3.5 * (m * k + k * n) + 7.0 * m * n, 7 * cdiv(mb, 128) * cdiv(nb, 128),
                                       sms, kEtaLcmaSingle, P, BW);
