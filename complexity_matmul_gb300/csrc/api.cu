@@ -163,11 +163,37 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   a.group_m = pair ? 8 : 16;
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
+  a.splits = 1;
+  a.kb_per_split = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
+  if (!pair) {
+    // Too few tiles to fill the machine (skinny M, small N): cut K into chunks
+    // of at least 8 slabs so that tiles x chunks approaches the SM count.
+    const int num_kb = a.kb_per_split;
+    const int cap = grid_cap(h);
+    if (tiles < cap / 2 && num_kb >= 16) {
+      int splits = std::min<int64_t>(cap / tiles, num_kb / 8);
+      splits = std::max(1, std::min(splits, 64));
+      if (splits > 1) {
+        const int kps = (num_kb + splits - 1) / splits;
+        splits = (num_kb + kps - 1) / kps;
+        const size_t part_bytes = static_cast<size_t>(tiles) * splits * kPlainBM * L.bn * sizeof(float);
+        const size_t ctr_bytes = static_cast<size_t>(tiles) * 4 * sizeof(int);
+        const size_t off = (part_bytes + 255) / 256 * 256;
+        int rc = ensure_workspace(h, off + ctr_bytes, st);
+        if (rc) return rc;
+        a.splits = splits;
+        a.kb_per_split = kps;
+        a.partial = static_cast<float*>(h->ws);
+        a.counters = reinterpret_cast<int*>(static_cast<char*>(h->ws) + off);
+        if (cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+      }
+    }
+  }
   if (pair) {
     L.grid = 2 * static_cast<int>(std::min<int64_t>(tiles, grid_cap(h) / 2));
     return launch_plain_pair(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
   }
-  L.grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap(h)));
+  L.grid = static_cast<int>(std::min<int64_t>(tiles * a.splits, grid_cap(h)));
   return launch_plain(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
 }
 

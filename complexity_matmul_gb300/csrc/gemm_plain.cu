@@ -45,6 +45,38 @@ __device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& m
   nb = local / rows;
 }
 
+// Cast 32 FP32 values of one C row and store them (columns col .. col+31, clipped to C).
+template <bool BF16>
+__device__ __forceinline__ void store_row_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
+                                                const PlainArgs& args) {
+  if (row >= args.M || col >= args.N) return;
+  if (col + 32 <= args.N) {
+    uint4* dst = reinterpret_cast<uint4*>(crow + col);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint4 o;
+      o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
+      o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
+      o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
+      o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
+      dst[v] = o;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
+      if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
+      if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
+    }
+  }
+}
+
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 template <int BN, int STAGES, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     plain_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -88,16 +120,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
   const int num_kb = (args.K + kBK - 1) / kBK;
+  const int num_work = args.num_tiles * args.splits;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+      for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+        const int tile = w / args.splits, split = w - tile * args.splits;
         int mb, nb;
         tile_coords(tile, args, mb, nb);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int kb0 = split * args.kb_per_split, kb1 = min(num_kb, kb0 + args.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
             ok = false;
             break;
@@ -129,14 +164,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+      for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
+        const int split = w % args.splits;
+        const int kb0 = split * args.kb_per_split, kb1 = min(num_kb, kb0 + args.kb_per_split);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, wc)) {
             ok = false;
             break;
@@ -146,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::kBBytes) >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           mma_commit(&empty[stage]);
           issued = true;
           if (++stage == STAGES) {
@@ -171,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t acc = 0, acc_phase = 0;
     uint16_t* Cp = static_cast<uint16_t*>(args.C);
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x) {
+    for (int w = blockIdx.x; w < num_work; w += gridDim.x) {
+      const int tile = w / args.splits, split = w - tile * args.splits;
       int mb, nb;
       tile_coords(tile, args, mb, nb);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc));
@@ -180,37 +218,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mb * kBM + q * 32 + lane;
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (args.splits == 1) {
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c * 32, r);
-        tmem_wait_ld();
-        const int col = nb * BN + c * 32;
-        if (row < args.M && col < args.N) {
-          if (col + 32 <= args.N) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + col);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          store_row_chunk<BF16>(crow, row, nb * BN + c * 32, r, args);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else {
+        // split-K: publish this chunk's FP32 partial (rows inside C only), free TMEM
+        float* mine = args.partial + ((static_cast<int64_t>(tile) * args.splits + split) * kBM + q * 32 + lane) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          if (row < args.M) {
+            uint4* dst = reinterpret_cast<uint4*>(mine + c * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
-              o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
-              o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
-              o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
-              dst[v] = o;
-            }
-          } else {
+            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        // The last chunk to arrive (per tile and lane quarter: no cross-warp
+        // barrier, no waiting) sums all chunks' partials in chunk order.
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atom_add_acq_rel(args.counters + tile * 4 + q, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == args.splits - 1) {
+          if (lane == 0) args.counters[tile * 4 + q] = 0;   // ready for the next launch
+          __threadfence();
+          const float* base = args.partial + (static_cast<int64_t>(tile) * args.splits * kBM + q * 32 + lane) * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            if (row >= args.M) break;
+            float acc32[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
-              if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
-              if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
+            for (int j = 0; j < 32; ++j) acc32[j] = 0.f;
+            for (int sp = 0; sp < args.splits; ++sp) {
+              const float4* src = reinterpret_cast<const float4*>(base + static_cast<int64_t>(sp) * kBM * BN + c * 32);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const float4 x = __ldcg(src + v);
+                acc32[4 * v] += x.x;
+                acc32[4 * v + 1] += x.y;
+                acc32[4 * v + 2] += x.z;
+                acc32[4 * v + 3] += x.w;
+              }
             }
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc32[j]);
+            store_row_chunk<BF16>(crow, row, nb * BN + c * 32, r, args);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

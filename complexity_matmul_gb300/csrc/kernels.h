@@ -19,6 +19,14 @@ struct PlainArgs {
   int group_m;          // tile rows per raster group (L2 reuse)
   int* err;             // device-visible error word
   uint64_t timeout_ns;  // bound on every mbarrier wait
+  // split-K (single-CTA kernel only): every tile's K range is cut into `splits`
+  // chunks of `kb_per_split` 64-deep slabs on consecutive work items; each
+  // chunk's FP32 partial goes to `partial`, and per tile and 32-row quarter the
+  // last chunk to finish (per `counters`) sums them in chunk order and writes C.
+  int splits;
+  int kb_per_split;
+  float* partial;       // [num_tiles][splits][128][BN]
+  int* counters;        // [num_tiles][4], zero before the launch
 };
 
 struct PlainLaunch {

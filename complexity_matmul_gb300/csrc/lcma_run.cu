@@ -14,6 +14,9 @@ namespace {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+}  // namespace
+
+// Grow the handle's workspace to at least `bytes` (stream-ordered with `st`).
 int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st) {
   if (bytes <= h->ws_bytes) return LCGEMM_OK;
   if (h->ws) {
@@ -30,6 +33,8 @@ int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st) {
   h->ws_bytes = bytes;
   return LCGEMM_OK;
 }
+
+namespace {
 
 template <int L>
 int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

@@ -33,6 +33,7 @@ bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uin
                 const uint64_t* strides_bytes, const uint32_t* box);
 bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows);
 int grid_cap(const lcgemm_ctx* h);
+int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st);
 
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st);

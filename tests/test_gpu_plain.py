@@ -118,6 +118,26 @@ def test_llm_skinny(h, M, N, K):
     assert_close(C, oracle_c64(A, B, "bf16", rows=rows), "bf16", "plain", rows=rows)
 
 
+# ---------------------------------------------------------------- split-K (few tiles, long K)
+
+SPLITK = [(1, 4096, 14336), (16, 1000, 2048), (100, 128, 4096), (1, 128, 4096), (128, 256, 8192), (3, 24, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SPLITK)
+def test_split_k_integer_bit_exact(h, M, N, K):
+    """Shapes with fewer tiles than SMs cut K into chunks; partial sums meet in FP32 (exact here)."""
+    A, B = synthetic.operands(M, N, K, "int3", 19, "bf16", "cuda")
+    ref = oracle_c64(A, B, "bf16")
+    for _ in range(3):                      # counters must be back at zero for every launch
+        assert_bit_exact(_run(h, A, B), ref, "bf16")
+
+
+def test_split_k_float(h):
+    A = synthetic.matrix(16, 14336, "normal", 1004, "bf16", "cuda")
+    B = synthetic.matrix(4096, 14336, "normal", 2004, "bf16", "cuda", scale=0.02)
+    assert_close(_run(h, A, B), oracle_c64(A, B, "bf16"), "bf16", "plain")
+
+
 # ---------------------------------------------------------------- identities and edge cases
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
