@@ -91,7 +91,8 @@ def _kernel_source_hash(name: str) -> str:
 
 
 def _traffic(kernel_file: str, n: int):
-    """DRAM bytes per launch from the committed ncu summary, if it still describes this source."""
+    """DRAM bytes per launch from a committed ncu summary of `kernel_file` at n^3, if that
+    summary was taken on the current source of the kernel (else None)."""
     prof = os.path.join(ROOT, "profiles")
     if not os.path.isdir(prof):
         return None
@@ -100,9 +101,9 @@ def _traffic(kernel_file: str, n: int):
         if not fn.endswith(".md"):
             continue
         text = open(os.path.join(prof, fn)).read()
-        for m in re.finditer(r"traffic_per_launch:\s*n=(\d+)\s+bytes=(\d+)\s+source=(\w+)", text):
-            if int(m.group(1)) == n and m.group(3) == want:
-                return int(m.group(2))
+        for m in re.finditer(r"traffic_per_launch:\s*kernel=(\S+)\s+n=(\d+)\s+bytes=(\d+)\s+source=(\w+)", text):
+            if m.group(1) == kernel_file and int(m.group(2)) == n and m.group(4) == want:
+                return int(m.group(3))
     return None
 
 
@@ -243,9 +244,10 @@ def run_gpu(args):
     dom_ms = statistics.mean(per_n_ms[dom])
     mma_frac = {"plain": 1.0, "strassen1": 7 / 8, "strassen2": 49 / 64}[dom_algo]
     achieved = mma_frac * 2.0 * dom ** 3 / (dom_ms * 1e-3) / 1e12
-    kernel_file = "gemm_plain.cu" if dom_algo == "plain" else "lcma_fused.cu"
-    traffic = _traffic(kernel_file, dom) if dom_algo == "plain" else None
-    roofline = {"bound": "tensor", "kernel": f"{dom_algo} GEMM {dom}^3", "achieved": round(achieved, 1),
+    # square shapes above 128 run the CTA-pair kernels (gemm_pair.cu, lcma_pair.cu)
+    kernel_file = {"plain": "gemm_pair.cu", "strassen1": "lcma_pair.cu", "strassen2": "lcma_fused.cu"}[dom_algo]
+    traffic = _traffic(kernel_file, dom)
+    roofline = {"bound": "tensor", "kernel": f"{dom_algo} GEMM {dom}^3 ({kernel_file})", "achieved": round(achieved, 1),
                 "peak": peak_burst, "unit": "TFLOP/s", "frac": round(achieved / peak_burst, 4),
                 "peak_source": f"{peak_kind} bf16 burst", "traffic": traffic}
 
