@@ -1,0 +1,88 @@
+"""The roofline cost model behind LCGEMM_AUTO, through a planning handle (CPU only, no CUDA call)."""
+import pytest
+
+import complexity_matmul_gb300 as lcg
+from complexity_matmul_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def plan():
+    _build.build()
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    yield h
+    h.close()
+
+
+def test_planning_handle_rejects_runs(plan):
+    assert plan.run_raw(8, 8, 8, None, 8, None, 8, None, 8, lcg.BF16, lcg.PLAIN) == lcg.ERR_ARG
+    assert plan.sync_status() == lcg.ERR_ARG
+
+
+def test_supported_dimensions(plan):
+    # one level: M, N even and K a multiple of 16; two levels: M, N multiples of 4 and K of 32
+    assert plan.estimate(130, 66, 48, lcg.BF16, "strassen1") > 0
+    with pytest.raises(lcg.LcgemmError) as e:
+        plan.estimate(131, 66, 48, lcg.BF16, "strassen1")
+    assert e.value.code == lcg.ERR_UNSUPPORTED
+    with pytest.raises(lcg.LcgemmError):
+        plan.estimate(128, 64, 40, lcg.BF16, "strassen1")
+    assert plan.estimate(132, 68, 64, lcg.BF16, "strassen2") > 0
+    with pytest.raises(lcg.LcgemmError):
+        plan.estimate(130, 68, 64, lcg.BF16, "strassen2")
+    with pytest.raises(lcg.LcgemmError):
+        plan.estimate(132, 68, 48, lcg.BF16, "strassen2")
+
+
+@pytest.mark.parametrize("shape", [(131, 257, 1000), (1, 4096, 4095), (4097, 4097, 4097), (64, 64, 8)])
+def test_auto_never_picks_an_unsupported_algorithm(plan, shape):
+    assert plan.select(*shape, lcg.BF16) == lcg.PLAIN
+
+
+def test_plain_estimate_grows_with_work(plan):
+    prev = 0.0
+    for n in (256, 1024, 2048, 4096, 8192, 16384):
+        t = plan.estimate(n, n, n, lcg.BF16, "plain")
+        assert t > prev
+        prev = t
+    # a compute-bound square GEMM runs within 2x of the tensor peak it is given
+    t = plan.estimate(16384, 16384, 16384, lcg.BF16, "plain")
+    assert 2 * 16384 ** 3 / 2.25e15 < t < 2 * 2 * 16384 ** 3 / 2.25e15
+
+
+def test_skinny_gemm_is_bandwidth_bound(plan):
+    M, N, K = 1, 14336, 4096
+    t = plan.estimate(M, N, K, lcg.BF16, "plain")
+    compulsory = 2.0 * (M * K + K * N + M * N) / 8e12
+    assert compulsory < t < 3 * compulsory
+
+
+def test_wave_quantisation(plan):
+    # 76 CTA pairs of 256x256 tiles: one more tile row than fits a wave costs a whole extra wave
+    full = plan.estimate(256 * 76, 256, 8192, lcg.BF16, "plain")
+    over = plan.estimate(256 * 77, 256, 8192, lcg.BF16, "plain")
+    assert over > 1.5 * full
+
+
+def test_strassen_saves_multiplies_only_when_large(plan):
+    # small shapes: the pre-pass and launches dominate, plain wins
+    for n in (256, 1024, 2048):
+        assert plan.select(n, n, n, lcg.BF16) == lcg.PLAIN
+        assert plan.estimate(n, n, n, lcg.BF16, "strassen1") > plan.estimate(n, n, n, lcg.BF16, "plain")
+    # the one-level model charges 7/8 of the multiplications plus 4.5(MK+KN) bytes of pre-pass
+    n = 65536
+    t1 = plan.estimate(n, n, n, lcg.BF16, "strassen1")
+    t0 = plan.estimate(n, n, n, lcg.BF16, "plain")
+    assert t1 < 1.2 * t0
+
+
+def test_peak_and_bandwidth_options_move_the_choice(plan):
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    n = 32768
+    base = h.estimate(n, n, n, lcg.BF16, "plain")
+    h.set_option(lcg.OPT_PEAK_GFLOPS, 4_500_000)     # twice the tensor peak: compute time halves
+    assert h.estimate(n, n, n, lcg.BF16, "plain") < 0.6 * base
+    h.set_option(lcg.OPT_HBM_GBPS, 100)              # starve the bandwidth: the pre-pass dominates
+    assert h.select(n, n, n, lcg.BF16) == lcg.PLAIN
+    with pytest.raises(lcg.LcgemmError):
+        h.set_option(lcg.OPT_PEAK_GFLOPS, 0)
+    h.close()
