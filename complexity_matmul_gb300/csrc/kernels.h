@@ -97,6 +97,7 @@ struct LcmaArgs {
   int split_first;                // items >= split_first are halves of split tail Groups
   int* flags;                     // one counter per split Group and CTA rank (zeroed before launch)
   int debug_drop;                 // test hook: second halves never publish
+  int raw2d;                      // CTA-pair path: raw-block maps are 2-D maps of the whole operand
   int64_t ldp;
   int num_products;
   int* err;

@@ -200,10 +200,19 @@ __device__ __forceinline__ void item_of(int w, const LcmaArgs& a, int& group, in
   }
 }
 
+// Operand tiles through 2-D maps (cheaper for the copy engine than 3-D / 4-D
+// boxes): summed operands as one (slots * rows_b) x kb matrix, and raw blocks
+// as the whole operand when raw2d is set (the block width kb is a multiple of
+// the 64-deep slab, so a slab never reaches into the next block); otherwise raw
+// blocks through the exact 4-D block map.  Rows past a block's end belong to
+// output rows outside C and are never stored.
 __device__ __forceinline__ void load_operand_pair(void* dst, const CUtensorMap* sum_map, const CUtensorMap* raw_map,
-                                                  const LcmaOperand& src, uint32_t bar, int k0, int row0) {
+                                                  const LcmaOperand& src, uint32_t bar, int k0, int row0, int rows_b,
+                                                  int kb, bool raw2d) {
   if (src.slot >= 0)
-    tma_load_3d_pair(dst, sum_map, bar, k0, row0, src.slot);
+    tma_load_2d_pair(dst, sum_map, bar, k0, src.slot * rows_b + row0);
+  else if (raw2d)
+    tma_load_2d_pair(dst, raw_map, bar, src.c * kb + k0, src.r * rows_b + row0);
   else
     tma_load_4d_pair(dst, raw_map, bar, k0, src.c, row0, src.r);
 }
@@ -359,9 +368,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (leader) mbar_arrive_expect_tx(&full[stage], kTxBytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
             load_operand_pair(sA + stage * kABytes, &tmA_sum, &tmA_raw, args_in.a_src[p], bar, kb * kBK,
-                              mb * 2 * kRows + static_cast<int>(rank) * kRows);
+                              mb * 2 * kRows + static_cast<int>(rank) * kRows, args_in.mb, args_in.kb, args_in.raw2d);
             load_operand_pair(sB + stage * kBBytes, &tmB_sum, &tmB_raw, args_in.b_src[p], bar, kb * kBK,
-                              nb * kTileN + static_cast<int>(rank) * (kTileN / 2));
+                              nb * kTileN + static_cast<int>(rank) * (kTileN / 2), args_in.nb, args_in.kb, args_in.raw2d);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {

@@ -70,23 +70,36 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   LcmaLaunch ll{};
   ll.levels = L;
   ll.bf16 = bf16;
+  // CTA-pair kernel: summed operands as one 2-D (slots * rows) x kb map; raw
+  // blocks as a 2-D map of the whole operand when kb is a multiple of 64.
+  const bool raw2d = pair && kb % 64 == 0;
   {
     const uint64_t dA[3] = {uint64_t(kb), uint64_t(mb), uint64_t(na)};
     const uint64_t sA[2] = {uint64_t(kb) * 2, uint64_t(mb * kb) * 2};
     const uint32_t boxA3[3] = {64u, 128u, 1u};
     const uint32_t boxB3[3] = {64u, uint32_t(b_box), 1u};
-    if (!encode_map(&ll.tmA_sum, bf16, wsA, 3, dA, sA, boxA3)) return LCGEMM_ERR_CUDA;
     const uint64_t dB[3] = {uint64_t(kb), uint64_t(nb), uint64_t(nbs)};
     const uint64_t sB[2] = {uint64_t(kb) * 2, uint64_t(nb * kb) * 2};
-    if (!encode_map(&ll.tmB_sum, bf16, wsB, 3, dB, sB, boxB3)) return LCGEMM_ERR_CUDA;
+    if (pair) {
+      if (!encode_kmajor(&ll.tmA_sum, bf16, wsA, int64_t(na) * mb, kb, kb, 128)) return LCGEMM_ERR_CUDA;
+      if (!encode_kmajor(&ll.tmB_sum, bf16, wsB, int64_t(nbs) * nb, kb, kb, b_box)) return LCGEMM_ERR_CUDA;
+    } else {
+      if (!encode_map(&ll.tmA_sum, bf16, wsA, 3, dA, sA, boxA3)) return LCGEMM_ERR_CUDA;
+      if (!encode_map(&ll.tmB_sum, bf16, wsB, 3, dB, sB, boxB3)) return LCGEMM_ERR_CUDA;
+    }
     const uint32_t boxA4[4] = {64u, 1u, 128u, 1u};
     const uint32_t boxB4[4] = {64u, 1u, uint32_t(b_box), 1u};
     const uint64_t rA[4] = {uint64_t(kb), uint64_t(G), uint64_t(mb), uint64_t(G)};
     const uint64_t rsA[3] = {uint64_t(kb) * 2, uint64_t(lda) * 2, uint64_t(mb * lda) * 2};
-    if (!encode_map(&ll.tmA_raw, bf16, A, 4, rA, rsA, boxA4)) return LCGEMM_ERR_CUDA;
     const uint64_t rB[4] = {uint64_t(kb), uint64_t(G), uint64_t(nb), uint64_t(G)};
     const uint64_t rsB[3] = {uint64_t(kb) * 2, uint64_t(ldb) * 2, uint64_t(nb * ldb) * 2};
-    if (!encode_map(&ll.tmB_raw, bf16, B, 4, rB, rsB, boxB4)) return LCGEMM_ERR_CUDA;
+    if (raw2d) {
+      if (!encode_kmajor(&ll.tmA_raw, bf16, A, M, K, lda, 128)) return LCGEMM_ERR_CUDA;
+      if (!encode_kmajor(&ll.tmB_raw, bf16, B, N, K, ldb, b_box)) return LCGEMM_ERR_CUDA;
+    } else {
+      if (!encode_map(&ll.tmA_raw, bf16, A, 4, rA, rsA, boxA4)) return LCGEMM_ERR_CUDA;
+      if (!encode_map(&ll.tmB_raw, bf16, B, 4, rB, rsB, boxB4)) return LCGEMM_ERR_CUDA;
+    }
   }
   LcmaArgs& a = ll.args;
   a.C = C;
@@ -121,6 +134,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
     a.num_items = split ? full_waves * P + 2 * rem : a.num_groups;
     a.flags = split ? reinterpret_cast<int*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes + s_bytes) : nullptr;
     a.debug_drop = h->debug_drop;
+    a.raw2d = raw2d ? 1 : 0;
     if (split && cudaMemsetAsync(a.flags, 0, sizeof(int) * 2 * rem, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     ll.grid = 2 * std::min(a.num_items, P);
     if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
