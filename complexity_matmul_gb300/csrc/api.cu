@@ -258,6 +258,10 @@ int lcgemm_destroy(lcgemm_t h) {
   cudaDeviceSynchronize();
   if (h->ws) cudaFree(h->ws);
   if (h->stage) cudaFree(h->stage);
+  for (int i = 0; i < lcgemm_ctx::kHostEvents; ++i)
+    if (h->ev[i]) cudaEventDestroy(h->ev[i]);
+  if (h->copy_in) cudaStreamDestroy(h->copy_in);
+  if (h->copy_out) cudaStreamDestroy(h->copy_out);
   if (h->err_host) cudaFreeHost(h->err_host);
   delete h;
   return LCGEMM_OK;
@@ -290,6 +294,12 @@ int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64
   return rc;
 }
 
+// Host buffers: B is copied first; A is copied in row chunks on a copy stream,
+// each chunk's GEMM runs on the caller's stream as soon as its rows arrive, and
+// each chunk of C goes back on a second copy stream -- host->device copies,
+// tensor-core work and device->host copies overlap.  Plain GEMMs (explicit or
+// chosen by the cost model) are chunked; a chunk of rows computes exactly what
+// the whole GEMM computes for those rows.  Strassen runs unchunked.
 int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
   if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;
@@ -309,6 +319,8 @@ int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, 
   if (need > h->stage_bytes) {
     if (h->stage) {
       cudaStreamSynchronize(st);
+      if (h->copy_in) cudaStreamSynchronize(h->copy_in);
+      if (h->copy_out) cudaStreamSynchronize(h->copy_out);
       cudaFree(h->stage);
       h->stage = nullptr;
       h->stage_bytes = 0;
@@ -322,15 +334,64 @@ int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, 
   char* dA = static_cast<char*>(h->stage);
   char* dB = dA + a_bytes;
   char* dC = dB + b_bytes;
-  if (K > 0) {
+  if (K == 0) {
+    rc = lcgemm_run(h, M, N, K, dA, kp, dB, kp, dC, np, dtype, algo, cuda_stream);
+    if (rc) return rc;
+    return cudaMemcpy2DAsync(C, ldc * 2, dC, np * 2, N * 2, M, cudaMemcpyDeviceToHost, st) == cudaSuccess
+               ? LCGEMM_OK
+               : LCGEMM_ERR_CUDA;
+  }
+  const int chosen = algo == LCGEMM_AUTO ? select_algo(h, M, N, K, dtype) : algo;
+  int chunks = 1;
+  if (chosen == LCGEMM_PLAIN) chunks = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, M / 2048)));
+  if (chunks == 1) {
     if (cudaMemcpy2DAsync(dA, kp * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpy2DAsync(dB, kp * 2, B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, st) != cudaSuccess)
       return LCGEMM_ERR_CUDA;
+    rc = lcgemm_run(h, M, N, K, dA, kp, dB, kp, dC, np, dtype, chosen, cuda_stream);
+    if (rc) return rc;
+    if (cudaMemcpy2DAsync(C, ldc * 2, dC, np * 2, N * 2, M, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+    return LCGEMM_OK;
   }
-  rc = lcgemm_run(h, M, N, K, dA, kp, dB, kp, dC, np, dtype, algo, cuda_stream);
-  if (rc) return rc;
-  if (cudaMemcpy2DAsync(C, ldc * 2, dC, np * 2, N * 2, M, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return LCGEMM_ERR_CUDA;
+  if (!h->copy_in) {
+    if (cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+    for (int i = 0; i < lcgemm_ctx::kHostEvents; ++i)
+      if (cudaEventCreateWithFlags(&h->ev[i], cudaEventDisableTiming) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  }
+  cudaEvent_t* ev = h->ev;   // [0] start, [1] B in, [2..2+c) A chunk in, [2+c..2+2c) C chunk done, [2+2c] out
+  const int64_t rows = ((M + chunks - 1) / chunks + 255) / 256 * 256;   // chunk rows, a multiple of 256
+  bool ok = cudaEventRecord(ev[0], st) == cudaSuccess && cudaStreamWaitEvent(h->copy_in, ev[0], 0) == cudaSuccess &&
+            cudaStreamWaitEvent(h->copy_out, ev[0], 0) == cudaSuccess;
+  ok = ok && cudaMemcpy2DAsync(dB, kp * 2, B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, h->copy_in) == cudaSuccess &&
+       cudaEventRecord(ev[1], h->copy_in) == cudaSuccess;
+  int n = 0;
+  for (int64_t r0 = 0; ok && r0 < M; r0 += rows, ++n) {
+    const int64_t mr = std::min(rows, M - r0);
+    ok = cudaMemcpy2DAsync(dA + r0 * kp * 2, kp * 2, static_cast<const char*>(A) + r0 * lda * 2, lda * 2, K * 2, mr,
+                           cudaMemcpyHostToDevice, h->copy_in) == cudaSuccess &&
+         cudaEventRecord(ev[2 + n], h->copy_in) == cudaSuccess;
+  }
+  ok = ok && cudaStreamWaitEvent(st, ev[1], 0) == cudaSuccess;
+  n = 0;
+  for (int64_t r0 = 0; ok && r0 < M; r0 += rows, ++n) {
+    const int64_t mr = std::min(rows, M - r0);
+    ok = cudaStreamWaitEvent(st, ev[2 + n], 0) == cudaSuccess;
+    if (ok) {
+      rc = lcgemm_run(h, mr, N, K, dA + r0 * kp * 2, kp, dB, kp, dC + r0 * np * 2, np, dtype, LCGEMM_PLAIN, cuda_stream);
+      if (rc) return rc;
+    }
+    ok = ok && cudaEventRecord(ev[2 + chunks + n], st) == cudaSuccess &&
+         cudaStreamWaitEvent(h->copy_out, ev[2 + chunks + n], 0) == cudaSuccess &&
+         cudaMemcpy2DAsync(static_cast<char*>(C) + r0 * ldc * 2, ldc * 2, dC + r0 * np * 2, np * 2, N * 2, mr,
+                           cudaMemcpyDeviceToHost, h->copy_out) == cudaSuccess;
+  }
+  ok = ok && cudaEventRecord(ev[2 + 2 * chunks], h->copy_out) == cudaSuccess &&
+       cudaStreamWaitEvent(st, ev[2 + 2 * chunks], 0) == cudaSuccess;
+  if (!ok) return LCGEMM_ERR_CUDA;
+  h->last_algo = LCGEMM_PLAIN;
   return LCGEMM_OK;
 }
 

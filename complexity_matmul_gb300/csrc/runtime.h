@@ -25,6 +25,10 @@ struct lcgemm_ctx {
   size_t ws_bytes = 0;
   void* stage = nullptr;        // staging for lcgemm_run_host
   size_t stage_bytes = 0;
+  // lcgemm_run_host pipeline: copy streams (host->device, device->host) and events
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  static constexpr int kHostEvents = 24;
+  cudaEvent_t ev[kHostEvents] = {};
 };
 
 namespace lcg {
