@@ -19,12 +19,11 @@ def h():
     handle.close()
 
 
-def _run_host(h, A, B, C, algo, lda=None, ldb=None, ldc=None):
-    M, K = A.shape[0], A.shape[1] if lda is None else lda
+def _run_host(h, A, B, C, algo):
+    """lcgemm_run_host on host tensors (A: M x K, B stored N x K, C: M x N; any row strides)."""
     sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    rc = h.run_host_raw(A.shape[0], B.shape[0], A.shape[1] if lda is None else K, A.data_ptr(),
-                        A.stride(0), B.data_ptr(), B.stride(0), C.data_ptr(), C.stride(0), lcg.BF16,
-                        lcg.ALGOS[algo], sp)
+    rc = h.run_host_raw(A.shape[0], B.shape[0], A.shape[1], A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+                        C.data_ptr(), C.stride(0), lcg.BF16, lcg.ALGOS[algo], sp)
     torch.cuda.synchronize()
     return rc
 
