@@ -190,7 +190,24 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     }
   }
   if (pair) {
-    L.grid = 2 * static_cast<int>(std::min<int64_t>(tiles, grid_cap(h) / 2));
+    // split the partial last wave into K halves when its tiles fit twice over
+    const int P = grid_cap(h) / 2;
+    const int full = a.num_tiles / P, rem = a.num_tiles - full * P;
+    const int num_kb = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
+    const bool split = h->split && rem > 0 && 2 * rem <= P && num_kb >= 8;
+    a.tail_first = split ? full * P : a.num_tiles;
+    a.num_items = split ? full * P + 2 * rem : a.num_tiles;
+    if (split) {
+      const size_t part_bytes = static_cast<size_t>(rem) * 2 * 256 * 256 * sizeof(float);
+      const size_t off = (part_bytes + 255) / 256 * 256;
+      const size_t ctr_bytes = static_cast<size_t>(rem) * 2 * 4 * sizeof(int);
+      int rc = ensure_workspace(h, off + ctr_bytes, st);
+      if (rc) return rc;
+      a.partial = static_cast<float*>(h->ws);
+      a.counters = reinterpret_cast<int*>(static_cast<char*>(h->ws) + off);
+      if (cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    }
+    L.grid = 2 * static_cast<int>(std::min<int64_t>(a.num_items, P));
     return launch_plain_pair(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
   }
   L.grid = static_cast<int>(std::min<int64_t>(tiles * a.splits, grid_cap(h)));

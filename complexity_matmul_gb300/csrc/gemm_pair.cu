@@ -8,6 +8,11 @@
 // reads 16 KB of A and 8 KB of (its half of) B per 64-deep K slab instead of
 // 16 KB + 32 KB, which halves the shared-memory and L2 traffic per flop.
 //
+// Tail split: when the tiles of the partial last wave fit twice over into the
+// pairs, each runs as two K halves on two pairs; each half publishes its FP32
+// partial and the second half to finish adds both (in half order) and casts.
+// Nobody waits for anybody.
+//
 // Synchronisation across the pair:
 //   full[s]   leader's barrier; the leader arms it with both CTAs' bytes and
 //             both CTAs' TMA copies complete on it
@@ -41,6 +46,57 @@ __device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& m
   const int local = tile - g * group_tiles;
   mb = first_m + local % rows;
   nb = local / rows;
+}
+
+// Work item -> tile and K-slab range.  Items below tail_first are whole tiles;
+// the rest are the two K halves of the tiles of the partial last wave.
+__device__ __forceinline__ void pair_item(int w, const PlainArgs& a, int num_kb, int& tile, int& kb0, int& kb1,
+                                          int& half) {
+  if (w < a.tail_first) {
+    tile = w;
+    kb0 = 0;
+    kb1 = num_kb;
+    half = -1;
+  } else {
+    const int i = (w - a.tail_first) >> 1;
+    half = (w - a.tail_first) & 1;
+    tile = a.tail_first + i;
+    const int mid = num_kb / 2;
+    kb0 = half ? mid : 0;
+    kb1 = half ? num_kb : mid;
+  }
+}
+
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Cast 32 FP32 values of one C row and store them (columns col .. col+31, clipped to C).
+template <bool BF16>
+__device__ __forceinline__ void store_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
+                                            const PlainArgs& args) {
+  if (row >= args.M || col >= args.N) return;
+  if (col + 32 <= args.N) {
+    uint4* dst = reinterpret_cast<uint4*>(crow + col);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint4 o;
+      o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
+      o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
+      o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
+      o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
+      dst[v] = o;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
+      if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
+      if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
+    }
+  }
 }
 
 template <bool BF16>
@@ -95,10 +151,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs) {
+      for (int w = pair; ok && w < args.num_items; w += num_pairs) {
+        int tile, kb0, kb1, half;
+        pair_item(w, args, num_kb, tile, kb0, kb1, half);
         int mb, nb;
         tile_coords(tile, args, mb, nb);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
             ok = false;
             break;
@@ -133,14 +191,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs) {
+      for (int w = pair; ok && w < args.num_items; w += num_pairs) {
+        int tile, kb0, kb1, half;
+        pair_item(w, args, num_kb, tile, kb0, kb1, half);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, wc)) {
             ok = false;
             break;
@@ -150,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           mma_commit_pair(&empty[stage]);
           issued = true;
           if (++stage == kStages) {
@@ -174,7 +234,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
     uint16_t* Cp = static_cast<uint16_t*>(args.C);
-    for (int tile = pair; tile < args.num_tiles; tile += num_pairs) {
+    for (int w = pair; w < args.num_items; w += num_pairs) {
+      int tile, kb0, kb1, half;
+      pair_item(w, args, num_kb, tile, kb0, kb1, half);
       int mb, nb;
       tile_coords(tile, args, mb, nb);
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc))) break;
@@ -182,37 +244,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int row = mb * 2 * kBM + rank * kBM + q * 32 + lane;
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+      if (half < 0) {
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c * 32, r);
-        tmem_wait_ld();
-        const int col = nb * kBN + c * 32;
-        if (row < args.M && col < args.N) {
-          if (col + 32 <= args.N) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + col);
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      } else {
+        // tail tile: publish this K half's FP32 partial, free the accumulator, and
+        // let the second half to arrive (per tile, CTA rank and lane quarter) sum both
+        const int i = tile - args.tail_first;
+        const int64_t slot_rows = int64_t(2) * kBM;   // per half: both ranks' 128 rows
+        float* mine = args.partial + ((int64_t(i) * 2 + half) * slot_rows + rank * kBM + q * 32 + lane) * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          if (row < args.M) {
+            uint4* dst = reinterpret_cast<uint4*>(mine + c * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
-              o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
-              o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
-              o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
-              dst[v] = o;
-            }
-          } else {
+            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        __threadfence();
+        __syncwarp();
+        int* ctr = args.counters + (i * 2 + static_cast<int>(rank)) * 4 + q;
+        int prev = 0;
+        if (lane == 0) prev = atom_add_acq_rel(ctr, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == 1) {
+          if (lane == 0) *ctr = 0;
+          __threadfence();
+          const float* p0 = args.partial + ((int64_t(i) * 2) * slot_rows + rank * kBM + q * 32 + lane) * kBN;
+          const float* p1 = p0 + slot_rows * kBN;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            if (row >= args.M) break;
+            uint32_t r[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
-              if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
-              if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
+            for (int v = 0; v < 8; ++v) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(p0 + c * 32) + v);
+              const float4 y = __ldcg(reinterpret_cast<const float4*>(p1 + c * 32) + v);
+              r[4 * v] = __float_as_uint(x.x + y.x);
+              r[4 * v + 1] = __float_as_uint(x.y + y.y);
+              r[4 * v + 2] = __float_as_uint(x.z + y.z);
+              r[4 * v + 3] = __float_as_uint(x.w + y.w);
             }
+            store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -27,6 +27,11 @@ struct PlainArgs {
   int kb_per_split;
   float* partial;       // [num_tiles][splits][128][BN]
   int* counters;        // [num_tiles][4], zero before the launch
+  // tail split (CTA-pair kernel only): work items below tail_first are whole tiles,
+  // the 2 * (num_tiles - tail_first) items after them are K halves of the last tiles
+  // (partials in `partial` as [tile][half][256][256], counters [tile][rank][4]).
+  int tail_first;
+  int num_items;
 };
 
 struct PlainLaunch {

@@ -82,7 +82,16 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
   if (algo == LCGEMM_PLAIN) {
     const double bytes = 2.0 * (m * k + k * n + m * n);
     const bool pair = sms >= 2 && (h->plain_kernel == 2 || (h->plain_kernel == 0 && M > 128 && N > 128));
-    if (pair) return kernel_time(mnk2, bytes, cdiv(M, 256) * cdiv(N, 256), sms / 2, kEtaPlainPair, P, BW);
+    if (pair) {
+      // the partial last wave runs as K halves when it fits twice over
+      const int64_t tiles = cdiv(M, 256) * cdiv(N, 256);
+      const int units = sms / 2;
+      const int64_t full = tiles / units, rem = tiles - full * units;
+      double eff = wave_efficiency(tiles, units);
+      if (h->split && rem > 0 && 2 * rem <= units && K >= 512)
+        eff = static_cast<double>(tiles) / ((static_cast<double>(full) + 0.5) * units);
+      return std::max(mnk2 / (kEtaPlainPair * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
+    }
     const int64_t bn = N <= 128 ? 128 : 256;
     return kernel_time(mnk2, bytes, cdiv(M, 128) * cdiv(N, bn), sms, kEtaPlainSingle, P, BW);
   }

@@ -138,6 +138,20 @@ def test_split_k_float(h):
     assert_close(_run(h, A, B), oracle_c64(A, B, "bf16"), "bf16", "plain")
 
 
+# ---------------------------------------------------------------- tail split of the CTA-pair kernel
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 512), (4352, 2560, 1000), (2304, 8448, 600)])
+def test_tail_split_integer_bit_exact(h, M, N, K):
+    """Tiles of a partial last wave run as two K halves on two pairs (summed by the later one)."""
+    A, B = synthetic.operands(M, N, K, "int3", 21, "bf16", "cuda")
+    rows = synthetic.row_sample(M, 256)
+    ref = oracle_c64(A, B, "bf16", rows=rows)
+    for split in (1, 0, 1):
+        h.set_option(lcg.OPT_SPLIT, split)
+        assert_bit_exact(_run(h, A, B), ref, "bf16", rows=rows)
+    h.set_option(lcg.OPT_SPLIT, 1)
+
+
 # ---------------------------------------------------------------- identities and edge cases
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
