@@ -315,8 +315,10 @@ int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64
 // each chunk's GEMM runs on the caller's stream as soon as its rows arrive, and
 // each chunk of C goes back on a second copy stream -- host->device copies,
 // tensor-core work and device->host copies overlap.  Plain GEMMs (explicit or
-// chosen by the cost model) are chunked; a chunk of rows computes exactly what
-// the whole GEMM computes for those rows.  Strassen runs unchunked.
+// chosen by the cost model) are chunked; a chunk may sum the K range in a
+// different FP32 order than the whole GEMM would (tail splits depend on the
+// tile count), so results agree to FP32 rounding, not bit for bit.  Strassen
+// runs unchunked.
 int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
   if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;

@@ -56,11 +56,18 @@ def test_skinny_gemm_is_bandwidth_bound(plan):
     assert compulsory < t < 3 * compulsory
 
 
-def test_wave_quantisation(plan):
-    # 76 CTA pairs of 256x256 tiles: one more tile row than fits a wave costs a whole extra wave
-    full = plan.estimate(256 * 76, 256, 8192, lcg.BF16, "plain")
-    over = plan.estimate(256 * 77, 256, 8192, lcg.BF16, "plain")
-    assert over > 1.5 * full
+def test_wave_quantisation():
+    """76 CTA pairs of 256x256 tiles: 80 tiles cost a second wave (or half of one when the
+    partial last wave is split into K halves)."""
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    K = 16384
+    full = h.estimate(1024, 256 * 19, K, lcg.BF16, "plain")     # 76 tiles: one full wave
+    over = h.estimate(1024, 256 * 20, K, lcg.BF16, "plain")     # 80 tiles
+    assert 1.3 * full < over < 1.7 * full
+    h.set_option(lcg.OPT_SPLIT, 0)
+    over_nosplit = h.estimate(1024, 256 * 20, K, lcg.BF16, "plain")
+    assert over_nosplit > 1.7 * full
+    h.close()
 
 
 def test_strassen_saves_multiplies_only_when_large(plan):
