@@ -140,7 +140,7 @@ def test_split_k_float(h):
 
 # ---------------------------------------------------------------- tail split of the CTA-pair kernel
 
-@pytest.mark.parametrize("M,N,K", [(4096, 4096, 512), (4352, 2560, 1000), (2304, 8448, 600)])
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 8192), (4352, 2560, 8200), (2560, 4352, 9000)])
 def test_tail_split_integer_bit_exact(h, M, N, K):
     """Tiles of a partial last wave run as two K halves on two pairs (summed by the later one)."""
     A, B = synthetic.operands(M, N, K, "int3", 21, "bf16", "cuda")
