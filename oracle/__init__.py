@@ -19,11 +19,15 @@ Contents
   (U, V, W) coefficient tables and applied in the three steps the write-up
   names for the basic GPU pipeline: combine A and B blocks, run the block
   products, combine the products into C (section "从 LCMA 到 FalconGEMM").
+* :mod:`oracle.epilogue` -- O3, the element-wise epilogue
+  ``D = act(C64 + bias) + residual`` in FP64 (DeepGEMM tuning blog, section
+  3.3; "Kernel 与性能", section "Fusion").
 
 Pins (``tests/test_oracle_*.py``): hand-computed golden products, A.I = A,
 linearity, agreement with numpy's matmul, exhaustive decoder checks, the Brent
-equations for the Strassen tables, a brute-force 2x2 check, and a recursive
-Strassen written independently of the tables.
+equations for the Strassen tables, a brute-force 2x2 check, a recursive
+Strassen written independently of the tables, hand-computed epilogues, normal
+table values of GELU and the tanh form's known gap to it.
 """
 from __future__ import annotations
 
@@ -140,6 +144,7 @@ def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
 
 from . import rounding  # noqa: E402  (re-exported submodules)
 from . import strassen  # noqa: E402
+from . import epilogue  # noqa: E402
 
 
 def reference_output(C64: np.ndarray, dtype: int) -> np.ndarray:
