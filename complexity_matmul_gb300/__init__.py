@@ -27,10 +27,12 @@ OK, ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_N
 ERR_TOO_LARGE = -8
 OPT_WAIT_TIMEOUT_US, OPT_GROUP_ORDER, OPT_SPLIT, OPT_MAX_CTAS = 1, 2, 3, 4
 OPT_PEAK_GFLOPS, OPT_HBM_GBPS, OPT_DEBUG_DROP_SIGNAL, OPT_PLAIN_KERNEL, OPT_LCMA_KERNEL = 5, 6, 7, 8, 9
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = 0, 1, 2, 3
+ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_GELU_TANH}
 
 EXPORTS = ("lcgemm_create", "lcgemm_destroy", "lcgemm_run", "lcgemm_run_host", "lcgemm_last_algo",
            "lcgemm_select", "lcgemm_estimate", "lcgemm_sync_status", "lcgemm_set_option",
-           "lcgemm_strerror", "lcgemm_strassen1_noalloc")
+           "lcgemm_strerror", "lcgemm_strassen1_noalloc", "lcgemm_run_epilogue")
 
 _lock = threading.Lock()
 _lib = None
@@ -40,6 +42,12 @@ class LcgemmError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         self.code = code
         super().__init__(f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})")
+
+
+class Epilogue(ctypes.Structure):
+    """``lcgemm_epilogue``: C = act(A.B + bias) + residual (device pointers or None)."""
+    _fields_ = [("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("ldr", ctypes.c_int64),
+                ("act", ctypes.c_int)]
 
 
 def lib_path() -> str:
@@ -65,6 +73,7 @@ def lib(build_if_missing: bool = False):
         run_args = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, vp]
         L.lcgemm_run.argtypes = run_args
         L.lcgemm_run_host.argtypes = run_args
+        L.lcgemm_run_epilogue.argtypes = run_args[:-1] + [ctypes.POINTER(Epilogue), vp]
         L.lcgemm_last_algo.argtypes = [vp]
         L.lcgemm_select.argtypes = [vp, i64, i64, i64, i32]
         L.lcgemm_estimate.argtypes = [vp, i64, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_double)]
@@ -113,6 +122,10 @@ def _algo_code(algo) -> int:
     return ALGOS[algo] if isinstance(algo, str) else int(algo)
 
 
+def _act_code(act) -> int:
+    return ACTS[act] if isinstance(act, str) else int(act)
+
+
 PLANNING_DEVICE = -1
 
 
@@ -155,6 +168,12 @@ class Handle:
         """``lcgemm_run`` with raw integers / pointers; returns the status code."""
         return self._lib.lcgemm_run(self._h, M, N, K, A, lda, B, ldb, C, ldc, dtype, _algo_code(algo), stream)
 
+    def run_epilogue_raw(self, M, N, K, A, lda, B, ldb, C, ldc, dtype, algo, bias=None, residual=None, ldr=0,
+                         act=ACT_NONE, stream=None) -> int:
+        ep = Epilogue(bias, residual, int(ldr), _act_code(act))
+        return self._lib.lcgemm_run_epilogue(self._h, M, N, K, A, lda, B, ldb, C, ldc, dtype, _algo_code(algo),
+                                             ctypes.byref(ep), stream)
+
     def run_host_raw(self, M, N, K, A, lda, B, ldb, C, ldc, dtype, algo, stream=None) -> int:
         return self._lib.lcgemm_run_host(self._h, M, N, K, A, lda, B, ldb, C, ldc, dtype, _algo_code(algo), stream)
 
@@ -177,13 +196,15 @@ class Handle:
         _check(self._lib.lcgemm_set_option(self._h, int(option), int(value)), "lcgemm_set_option")
 
     # torch convenience -----------------------------------------------------
-    def run(self, A, Bnk, C=None, algo="plain", stream=None):
-        """C = A . B for torch CUDA tensors.
+    def run(self, A, Bnk, C=None, algo="plain", stream=None, bias=None, residual=None, act="none"):
+        """C = act(A . B + bias) + residual for torch CUDA tensors.
 
         ``A``: M x K (row stride >= K, unit column stride); ``Bnk``: the K x N
         operand stored as N x K (the column-major layout of B); ``C``: M x N
-        output (allocated if None).  Runs on ``stream`` (default: torch's
-        current stream).  Returns C.
+        output (allocated if None); ``bias``: N values or None; ``residual``:
+        M x N (may be ``C`` itself) or None; ``act``: "none", "relu", "gelu" or
+        "gelu_tanh".  Runs on ``stream`` (default: torch's current stream).
+        Returns C.
         """
         import torch
         if A.dim() != 2 or Bnk.dim() != 2 or A.shape[1] != Bnk.shape[1]:
@@ -202,9 +223,21 @@ class Handle:
         if stream is None:
             stream = torch.cuda.current_stream(A.device)
         sp = ctypes.c_void_p(stream.cuda_stream)
-        rc = self.run_raw(M, N, K, A.data_ptr(), _ld(A), Bnk.data_ptr(), _ld(Bnk), C.data_ptr(), _ld(C),
-                          _dtype_code(A), _algo_code(algo), sp)
-        _check(rc, "lcgemm_run")
+        args = (M, N, K, A.data_ptr(), _ld(A), Bnk.data_ptr(), _ld(Bnk), C.data_ptr(), _ld(C), _dtype_code(A),
+                _algo_code(algo))
+        if bias is None and residual is None and _act_code(act) == ACT_NONE:
+            _check(self.run_raw(*args, sp), "lcgemm_run")
+            return C
+        if bias is not None and (bias.dtype != A.dtype or bias.dim() != 1 or bias.shape[0] != N
+                                 or bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous vector of N values of the input dtype")
+        if residual is not None and (residual.dtype != A.dtype or tuple(residual.shape) != (M, N)
+                                     or residual.stride(1) != 1):
+            raise ValueError("residual must be M x N of the input dtype with unit column stride")
+        rc = self.run_epilogue_raw(*args, bias=None if bias is None else bias.data_ptr(),
+                                   residual=None if residual is None else residual.data_ptr(),
+                                   ldr=0 if residual is None else _ld(residual), act=act, stream=sp)
+        _check(rc, "lcgemm_run_epilogue")
         return C
 
 
@@ -218,6 +251,6 @@ def default_handle(device: int = 0) -> Handle:
     return h
 
 
-def gemm(A, Bnk, algo="plain", out=None):
-    """C = A . B on A's device with the per-device default handle."""
-    return default_handle(A.device.index or 0).run(A, Bnk, out, algo)
+def gemm(A, Bnk, algo="plain", out=None, bias=None, residual=None, act="none"):
+    """C = act(A . B + bias) + residual on A's device with the per-device default handle."""
+    return default_handle(A.device.index or 0).run(A, Bnk, out, algo, bias=bias, residual=residual, act=act)

@@ -116,6 +116,30 @@ int check_device_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t ld
   return LCGEMM_OK;
 }
 
+// Checks the caller's epilogue against C and converts it for the kernels.
+int make_epilogue(const lcgemm_epilogue* in, int64_t M, int64_t N, const void* C, int64_t ldc, lcg::Epilogue* out) {
+  *out = lcg::Epilogue{};
+  if (!in) return LCGEMM_OK;
+  if (in->act < LCGEMM_ACT_NONE || in->act > LCGEMM_ACT_GELU_TANH) return LCGEMM_ERR_ARG;
+  const int64_t c_bytes = ((M - 1) * ldc + N) * 2;
+  if (in->bias) {
+    if (reinterpret_cast<uintptr_t>(in->bias) & 15u) return LCGEMM_ERR_ALIGN;
+    if (overlaps(C, c_bytes, in->bias, N * 2)) return LCGEMM_ERR_ALIAS;
+  }
+  if (in->residual) {
+    if (in->ldr < N || in->ldr > (int64_t(1) << 36)) return LCGEMM_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(in->residual) & 15u) || (in->ldr & 7)) return LCGEMM_ERR_ALIGN;
+    const bool in_place = in->residual == C && in->ldr == ldc;
+    if (!in_place && overlaps(C, c_bytes, in->residual, ((M - 1) * in->ldr + N) * 2)) return LCGEMM_ERR_ALIAS;
+  }
+  out->bias = static_cast<const uint16_t*>(in->bias);
+  out->residual = static_cast<const uint16_t*>(in->residual);
+  out->ldr = in->residual ? in->ldr : 0;
+  out->act = in->act;
+  out->on = (in->bias || in->residual || in->act != LCGEMM_ACT_NONE) ? 1 : 0;
+  return LCGEMM_OK;
+}
+
 int take_error(lcgemm_ctx* h) {
   volatile int* e = h->err_host;
   const int v = *e;
@@ -141,7 +165,7 @@ int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N) {
 }
 
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-              int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
+              int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
   PlainLaunch L{};
   L.bf16 = bf16;
   const bool pair = plain_variant(h, M, N) == 2;
@@ -163,6 +187,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   a.group_m = pair ? 8 : 16;
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
+  a.ep = ep;
   a.splits = 1;
   a.kb_per_split = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
   if (!pair) {
@@ -288,27 +313,41 @@ int lcgemm_destroy(lcgemm_t h) {
 
 int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
+  return lcgemm_run_epilogue(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, algo, nullptr, cuda_stream);
+}
+
+int lcgemm_run_epilogue(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                        int64_t ldb, void* C, int64_t ldc, int dtype, int algo, const lcgemm_epilogue* epilogue,
+                        void* cuda_stream) {
   if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;
   int rc = check_shape(M, N, K, dtype, algo);
   if (rc) return rc;
   if (M == 0 || N == 0) return LCGEMM_OK;
   rc = check_device_args(M, N, K, A, lda, B, ldb, C, ldc);
   if (rc) return rc;
+  lcg::Epilogue ep;
+  rc = make_epilogue(epilogue, M, N, C, ldc, &ep);
+  if (rc) return rc;
   rc = take_error(h);
   if (rc) return rc;
   DeviceGuard g(h->device);
   if (!g.ok) return LCGEMM_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const bool bf16 = dtype == LCGEMM_BF16;
   if (K == 0) {
-    if (cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(N) * 2, static_cast<size_t>(M),
-                          st) != cudaSuccess)
+    if (ep.on) {
+      if (launch_epilogue_only(C, ldc, static_cast<int>(M), static_cast<int>(N), ep, bf16, h->num_sms, st) !=
+          cudaSuccess)
+        return LCGEMM_ERR_CUDA;
+    } else if (cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(N) * 2,
+                                 static_cast<size_t>(M), st) != cudaSuccess) {
       return LCGEMM_ERR_CUDA;
+    }
     h->last_algo = LCGEMM_PLAIN;
     return LCGEMM_OK;
   }
-  const bool bf16 = dtype == LCGEMM_BF16;
   int chosen = algo == LCGEMM_AUTO ? select_algo(h, M, N, K, dtype) : algo;
-  rc = dispatch(h, chosen, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+  rc = dispatch(h, chosen, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
   if (rc == LCGEMM_OK) h->last_algo = chosen;
   return rc;
 }
@@ -495,7 +534,7 @@ const char* lcgemm_strerror(int code) {
     case LCGEMM_ERR_ARG: return "invalid argument";
     case LCGEMM_ERR_ALIGN: return "pointer not 16-byte aligned or leading dimension not a multiple of 8";
     case LCGEMM_ERR_UNSUPPORTED: return "algorithm does not support these dimensions";
-    case LCGEMM_ERR_ALIAS: return "C overlaps A or B";
+    case LCGEMM_ERR_ALIAS: return "C overlaps A, B or the bias, or partly overlaps the residual";
     case LCGEMM_ERR_CUDA: return "CUDA call or kernel launch failed";
     case LCGEMM_ERR_TIMEOUT: return "a bounded device-side wait gave up in an earlier launch";
     case LCGEMM_ERR_NOMEM: return "workspace allocation failed";

@@ -15,6 +15,7 @@
 // it into the product kernel's epilogue instead.
 #include <utility>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "lcma_tables.h"
 #include "ptx.cuh"
@@ -126,13 +127,10 @@ __global__ void __launch_bounds__(256) combine_h_kernel(const __grid_constant__ 
           acc[2] += w * m.z;
           acc[3] += w * m.w;
         }
-        uint16_t* crow = a.C + (br * int64_t(a.mb) + i) * a.ldc + bc * int64_t(a.nb);
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const uint32_t pk = pack2(acc[e], acc[e + 1], BF16);
-          if (j + e < a.nb) crow[j + e] = static_cast<uint16_t>(pk & 0xffffu);
-          if (j + e + 1 < a.nb) crow[j + e + 1] = static_cast<uint16_t>(pk >> 16);
-        }
+        const int64_t row = br * int64_t(a.mb) + i;
+        uint16_t* crow = a.C + row * a.ldc + bc * int64_t(a.nb);
+        const int n = static_cast<int>(a.nb - j < 4 ? a.nb - j : 4);
+        store_run<BF16, 4>(crow + j, row, bc * int64_t(a.nb) + j, n, acc, a.ep);
       }
   }
 }

@@ -1,0 +1,135 @@
+// The fused element-wise epilogue and the one rounding of C.
+//
+// Every kernel that finishes an output element hands a run of W consecutive
+// FP32 values of one C row to store_run(): it applies
+//
+//     D = act(acc + bias[col]) + residual[row, col]
+//
+// in FP32 while the values are still in registers, rounds D once to the
+// output type (round to nearest even) and stores it.  This is the fusion the
+// DeepGEMM tuning blog describes in section 3.3 (bias broadcast onto the
+// finished tile, a tanh-approximated GeLU, then the store) and the "bias +
+// activation" / "residual" fusions of the "Fusion" section of "Kernel 与性能"
+// (wineandchord.com kernels-performance): the epilogue costs no extra pass
+// over C.
+//
+// GELU_TANH evaluates tanh with the hardware approximation (tanh.approx.f32),
+// the fast tanh the DeepGEMM blog uses; GELU calls CUDA's erfcf.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lcg {
+
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float activate(float x, int act) {
+  if (act == kActRelu) return x > 0.f ? x : 0.f;
+  // x Phi(x) = x/2 erfc(-x / sqrt 2): erfc keeps its relative accuracy in the
+  // negative tail, where 1 + erf(x / sqrt 2) would cancel
+  if (act == kActGelu) return 0.5f * x * erfcf(-x * 0.70710678118654752f);
+  if (act == kActGeluTanh) {
+    // sqrt(2/pi) * (x + 0.044715 x^3)
+    const float u = 0.79788456080286536f * fmaf(0.044715f * x, x * x, x);
+    return 0.5f * x * (1.f + tanh_hw(u));
+  }
+  return x;
+}
+
+// Two 16-bit values (low half first) of the output type to FP32.
+template <bool BF16>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+  if (BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = f.x;
+    hi = f.y;
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float unpack1(uint16_t b) {
+  return BF16 ? __uint_as_float(static_cast<uint32_t>(b) << 16) : __half2float(__ushort_as_half(b));
+}
+
+// Adds W values of a 16-bit vector starting at p (16-byte aligned when vec) to v.
+// RO: read through the read-only path (the bias, which no thread writes);
+// otherwise a streaming load (the residual, read once, and possibly C itself).
+template <bool BF16, int W, bool RO>
+__device__ __forceinline__ void add_run(float (&v)[W], const uint16_t* p, int n, bool vec) {
+  if (W % 8 == 0 && vec) {
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+      const uint4* src = reinterpret_cast<const uint4*>(p) + q;
+      const uint4 u = RO ? __ldg(src) : __ldcs(src);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float lo, hi;
+        unpack2<BF16>(w[t], lo, hi);
+        v[8 * q + 2 * t] += lo;
+        v[8 * q + 2 * t + 1] += hi;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+      if (j < n) v[j] += unpack1<BF16>(p[j]);
+  }
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// Epilogue + cast + store of v[0 .. n) = C[row, col .. col + n) (n <= W; the
+// values past n are ignored).  dst points at C[row, col].
+template <bool BF16, int W>
+__device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t col, int n, float (&v)[W],
+                                          const Epilogue& e) {
+  const bool full = n == W;
+  if (e.on) {
+    if (e.bias) {
+      const uint16_t* bp = e.bias + col;
+      add_run<BF16, W, true>(v, bp, n, full && aligned16(bp));
+    }
+    if (e.act) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) v[j] = activate(v[j], e.act);
+    }
+    if (e.residual) {
+      const uint16_t* rp = e.residual + row * e.ldr + col;
+      add_run<BF16, W, false>(v, rp, n, full && aligned16(rp));
+    }
+  }
+  if (W % 8 == 0 && full && aligned16(dst)) {
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+      uint4 o;
+      o.x = pack2(v[8 * q + 0], v[8 * q + 1], BF16);
+      o.y = pack2(v[8 * q + 2], v[8 * q + 3], BF16);
+      o.z = pack2(v[8 * q + 4], v[8 * q + 5], BF16);
+      o.w = pack2(v[8 * q + 6], v[8 * q + 7], BF16);
+      reinterpret_cast<uint4*>(dst)[q] = o;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; j += 2) {
+      const uint32_t p = pack2(v[j], j + 1 < W ? v[j + 1] : 0.f, BF16);
+      if (j < n) dst[j] = static_cast<uint16_t>(p & 0xffffu);
+      if (j + 1 < n) dst[j + 1] = static_cast<uint16_t>(p >> 16);
+    }
+  }
+}
+
+}  // namespace lcg

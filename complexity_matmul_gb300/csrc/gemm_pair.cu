@@ -19,6 +19,7 @@
 //   empty[s]  one per CTA; the leader's MMA commit arrives on both
 //   tfull[b]  one per CTA; the leader's MMA commit arrives on both
 //   tempty[b] leader's barrier; all 8 epilogue warps of the pair arrive
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -73,30 +74,15 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
   return old;
 }
 
-// Cast 32 FP32 values of one C row and store them (columns col .. col+31, clipped to C).
+// Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
 template <bool BF16>
 __device__ __forceinline__ void store_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
                                             const PlainArgs& args) {
   if (row >= args.M || col >= args.N) return;
-  if (col + 32 <= args.N) {
-    uint4* dst = reinterpret_cast<uint4*>(crow + col);
+  float v[32];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      uint4 o;
-      o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
-      o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
-      o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
-      o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
-      dst[v] = o;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
-      if (col + j < args.N) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
-      if (col + j + 1 < args.N) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
-    }
-  }
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep);
 }
 
 template <bool BF16>

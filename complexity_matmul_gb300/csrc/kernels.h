@@ -8,6 +8,18 @@
 
 namespace lcg {
 
+// Fused element-wise epilogue D = act(acc + bias[col]) + residual[row, col],
+// applied in FP32 by whichever kernel finishes an output element, before the
+// one rounding to the output type (epilogue.cuh).
+enum : int { kActNone = 0, kActRelu = 1, kActGelu = 2, kActGeluTanh = 3 };
+struct Epilogue {
+  const uint16_t* bias;      // N values of the output type, 16-byte aligned, or null
+  const uint16_t* residual;  // M x N of the output type, rows ldr apart (16-byte aligned), or null
+  int64_t ldr;               // elements, a multiple of 8
+  int act;                   // kActNone .. kActGeluTanh
+  int on;                    // any of bias, residual, act present
+};
+
 // Arguments of the persistent plain GEMM: C[M,N] = A[M,K] . B[K,N].
 // A and B are read through tensor maps (K-major, 128-byte swizzled boxes of
 // 64 x 128 resp. 64 x BN elements); C is written directly.
@@ -32,6 +44,7 @@ struct PlainArgs {
   // (partials in `partial` as [tile][half][256][256], counters [tile][rank][4]).
   int tail_first;
   int num_items;
+  Epilogue ep;
 };
 
 struct PlainLaunch {
@@ -77,6 +90,7 @@ struct CombineHArgs {
   uint16_t* C;
   int64_t ldc;
   int mb, nb;
+  Epilogue ep;          // applied in C's coordinates
 };
 cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st);
 
@@ -107,6 +121,7 @@ struct LcmaArgs {
   int num_products;
   int* err;
   uint64_t timeout_ns;
+  Epilogue ep;                    // applied in C's coordinates when a value is final
 };
 
 struct LcmaLaunch {
@@ -122,5 +137,9 @@ cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st);
 // boxes; quadrant sums in a per-CTA FP32 scratch of lcma_pair_scratch_bytes(grid) bytes.
 cudaError_t launch_lcma_pair(const LcmaLaunch& L, cudaStream_t st);
 size_t lcma_pair_scratch_bytes(int grid);
+
+// K = 0 with an epilogue: C = act(bias) + residual (the product is empty).
+cudaError_t launch_epilogue_only(void* C, int64_t ldc, int M, int N, const Epilogue& ep, bool bf16, int num_sms,
+                                 cudaStream_t st);
 
 }  // namespace lcg

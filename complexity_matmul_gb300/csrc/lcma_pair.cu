@@ -266,32 +266,14 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += __ldcg(pp + j * kRows);
         }
-        // cast once and store into quadrant t.quad of C
+        // epilogue, cast once and store into quadrant t.quad of C
         const int qr = t.quad >> 1, qc = t.quad & 1;
-        uint16_t* crow = Cp + (static_cast<int64_t>(qr) * a.mb + rloc) * a.ldc + static_cast<int64_t>(qc) * a.nb;
+        const int64_t crow_i = static_cast<int64_t>(qr) * a.mb + rloc;
+        uint16_t* crow = Cp + crow_i * a.ldc + static_cast<int64_t>(qc) * a.nb;
         const int qcol = tile_col0 + col;              // column inside the quadrant
-        if (rloc < a.mb && qcol < a.nb) {
-          const bool vec = (qcol + 32 <= a.nb) && ((reinterpret_cast<uintptr_t>(crow + qcol) & 15u) == 0);
-          if (vec) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + qcol);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint4 o;
-              o.x = pack2(v[8 * w + 0], v[8 * w + 1], BF16);
-              o.y = pack2(v[8 * w + 2], v[8 * w + 3], BF16);
-              o.z = pack2(v[8 * w + 4], v[8 * w + 5], BF16);
-              o.w = pack2(v[8 * w + 6], v[8 * w + 7], BF16);
-              dst[w] = o;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const uint32_t p = pack2(v[j], v[j + 1], BF16);
-              if (qcol + j < a.nb) crow[qcol + j] = static_cast<uint16_t>(p & 0xffffu);
-              if (qcol + j + 1 < a.nb) crow[qcol + j + 1] = static_cast<uint16_t>(p >> 16);
-            }
-          }
-        }
+        if (rloc < a.mb && qcol < a.nb)
+          store_run<BF16, 32>(crow + qcol, crow_i, static_cast<int64_t>(qc) * a.nb + qcol, min(32, a.nb - qcol), v,
+                              a.ep);
       }
     }
   }

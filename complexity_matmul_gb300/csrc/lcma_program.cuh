@@ -3,6 +3,7 @@
 // kernels.  See lcma_fused.cu for the schedule and its rationale.
 #pragma once
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "lcma_tables.h"
 #include "ptx.cuh"
@@ -154,14 +155,15 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t targe
   }
 }
 
-// Cast one warp's 32 rows x 128 columns of a TMEM buffer and store them into
-// quadrant `quad` of C.  `rloc`: this thread's row inside the quadrant;
-// `col0`: the tile's first column inside the quadrant.
+// Epilogue, cast and store of one warp's 32 rows x 128 columns of a TMEM
+// buffer into quadrant `quad` of C.  `rloc`: this thread's row inside the
+// quadrant; `col0`: the tile's first column inside the quadrant.
 template <bool BF16>
 __device__ __forceinline__ void store_quadrant(uint32_t tsrc, const LcmaArgs& a, int quad, int rloc, int col0) {
   const int qr = quad >> 1, qc = quad & 1;
   uint16_t* Cp = static_cast<uint16_t*>(a.C);
-  uint16_t* crow = Cp + (static_cast<int64_t>(qr) * a.mb + rloc) * a.ldc + static_cast<int64_t>(qc) * a.nb;
+  const int64_t row = static_cast<int64_t>(qr) * a.mb + rloc;
+  uint16_t* crow = Cp + row * a.ldc + static_cast<int64_t>(qc) * a.nb;
 #pragma unroll 1
   for (int c = 0; c < kBufCols / 32; ++c) {
     uint32_t r[32];
@@ -169,26 +171,10 @@ __device__ __forceinline__ void store_quadrant(uint32_t tsrc, const LcmaArgs& a,
     tmem_wait_ld();
     const int col = col0 + c * 32;
     if (rloc < a.mb && col < a.nb) {
-      const bool vec = (col + 32 <= a.nb) && ((reinterpret_cast<uintptr_t>(crow + col) & 15u) == 0);
-      if (vec) {
-        uint4* dst = reinterpret_cast<uint4*>(crow + col);
+      float v[32];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 o;
-          o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), BF16);
-          o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), BF16);
-          o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), BF16);
-          o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), BF16);
-          dst[v] = o;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const uint32_t p = pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), BF16);
-          if (col + j < a.nb) crow[col + j] = static_cast<uint16_t>(p & 0xffffu);
-          if (col + j + 1 < a.nb) crow[col + j + 1] = static_cast<uint16_t>(p >> 16);
-        }
-      }
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      store_run<BF16, 32>(crow + col, row, static_cast<int64_t>(qc) * a.nb + col, min(32, a.nb - col), v, a.ep);
     }
   }
 }

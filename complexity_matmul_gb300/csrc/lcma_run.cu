@@ -38,7 +38,7 @@ namespace {
 
 template <int L>
 int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-               const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
+               const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
   constexpr LcmaPlan<L> plan{};
   constexpr int G = plan.G;
   const int64_t mb = M / G, nb = N / G, kb = K / G;
@@ -124,6 +124,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   a.num_products = plan.R;
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
+  a.ep = ep;
   if (pair) {
     // Stream-K style split of the tail: when the last, partial wave of Groups
     // fits twice over, its Groups run as two halves on two pairs each.
@@ -147,7 +148,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   }
   ll.grid = std::min(a.num_groups * plan.R, grid_cap(h));
   if (launch_lcma_products(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
-  CombineHArgs ch{prod, ldp, static_cast<uint16_t*>(C), ldc, static_cast<int>(mb), static_cast<int>(nb)};
+  CombineHArgs ch{prod, ldp, static_cast<uint16_t*>(C), ldc, static_cast<int>(mb), static_cast<int>(nb), ep};
   if (launch_combine_h(ch, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
   return LCGEMM_OK;
 }
@@ -155,9 +156,10 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
 }  // namespace
 
 int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, int64_t K, const void* A,
-                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
-  if (levels == 1) return run_levels<1>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
-  if (levels == 2) return run_levels<2>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep,
+                 cudaStream_t st) {
+  if (levels == 1) return run_levels<1>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
+  if (levels == 2) return run_levels<2>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
   return LCGEMM_ERR_UNSUPPORTED;
 }
 

@@ -146,17 +146,17 @@ int select_algo(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, int dtype)
 }
 
 int dispatch(lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-             int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st) {
+             int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
   if (!algo_supported(algo, M, N, K)) return LCGEMM_ERR_UNSUPPORTED;
   switch (algo) {
     case LCGEMM_PLAIN:
-      return run_plain(h, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+      return run_plain(h, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
     case LCGEMM_STRASSEN1:
-      return run_strassen(h, 1, true, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+      return run_strassen(h, 1, true, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
     case LCGEMM_STRASSEN1_UNFUSED:
-      return run_strassen(h, 1, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+      return run_strassen(h, 1, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
     case LCGEMM_STRASSEN2:
-      return run_strassen(h, 2, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, st);
+      return run_strassen(h, 2, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
     default:
       return LCGEMM_ERR_UNSUPPORTED;
   }

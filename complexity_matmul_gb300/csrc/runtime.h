@@ -39,17 +39,20 @@ bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, in
 int grid_cap(const lcgemm_ctx* h);
 int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st);
 
+struct Epilogue;
+
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-              int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st);
+              int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st);
 
 int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, int64_t K, const void* A,
-                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st);
+                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep,
+                 cudaStream_t st);
 
 // Dispatcher and cost model (runtime.cu).
 bool algo_supported(int algo, int64_t M, int64_t N, int64_t K);
 int select_algo(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, int dtype);
 double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K);
 int dispatch(lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-             int64_t ldb, void* C, int64_t ldc, bool bf16, cudaStream_t st);
+             int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st);
 
 }  // namespace lcg

@@ -144,6 +144,55 @@ LCGEMM_API int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K,
                     const void* A, int64_t lda, const void* B, int64_t ldb,
                     void* C, int64_t ldc, int dtype, int algo, void* cuda_stream);
 
+/* activation of the fused epilogue (lcgemm_epilogue.act) */
+enum {
+  LCGEMM_ACT_NONE = 0,
+  LCGEMM_ACT_RELU = 1,       /* x > 0 ? x : +0                                             */
+  LCGEMM_ACT_GELU = 2,       /* x * Phi(x) = x/2 (1 + erf(x / sqrt 2))                     */
+  LCGEMM_ACT_GELU_TANH = 3   /* x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), hardware
+                                tanh approximation (absolute error of tanh below 2^-10)   */
+};
+
+/*
+ * Element-wise epilogue fused into the GEMM (DeepGEMM tuning blog, kwkr.cn
+ * news 553926, section 3.3: bias add and GeLU applied to the finished tile in
+ * registers before the single store; "Kernel 与性能", wineandchord.com
+ * kernels-performance, section "Fusion": bias + activation, residual add):
+ *
+ *     C[i,j] = act( sum_k A[i,k] B[k,j] + bias[j] ) + residual[i,j]
+ *
+ * evaluated in FP32 from the FP32 accumulator and rounded once to dtype.
+ *   bias     : device pointer to N values of dtype (one per column of C), or
+ *              NULL; 16-byte aligned; must not overlap C.
+ *   residual : device pointer to an M x N matrix of dtype, element (i,j) at
+ *              residual[i*ldr + j], or NULL; 16-byte aligned, ldr >= N and a
+ *              multiple of 8.  It may be C itself (same pointer, ldr == ldc:
+ *              an in-place residual add); any other overlap with C is
+ *              LCGEMM_ERR_ALIAS.
+ *   act      : LCGEMM_ACT_*.
+ * Both buffers are owned by the caller and only read.
+ */
+typedef struct {
+  const void* bias;
+  const void* residual;
+  int64_t ldr;
+  int act;
+} lcgemm_epilogue;
+
+/*
+ * lcgemm_run with a fused epilogue (`ep` NULL or all-empty: plain lcgemm_run).
+ * Every algorithm applies it where an element of C becomes final: the plain
+ * kernels after the K loop (or the split-K / split-tail sum), the Strassen
+ * kernels after the quadrant recombination.  K = 0 gives act(bias) + residual.
+ * Errors: those of lcgemm_run, plus LCGEMM_ERR_ARG for an unknown act or a
+ * residual with ldr < N, LCGEMM_ERR_ALIGN for a misaligned bias / residual or
+ * an ldr that is not a multiple of 8, LCGEMM_ERR_ALIAS as stated above.
+ */
+LCGEMM_API int lcgemm_run_epilogue(lcgemm_t h, int64_t M, int64_t N, int64_t K,
+                        const void* A, int64_t lda, const void* B, int64_t ldb,
+                        void* C, int64_t ldc, int dtype, int algo,
+                        const lcgemm_epilogue* ep, void* cuda_stream);
+
 /* Algorithm the last successful lcgemm_run on this handle executed (LCGEMM_PLAIN..). */
 LCGEMM_API int lcgemm_last_algo(lcgemm_t h);
 

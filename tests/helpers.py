@@ -67,3 +67,60 @@ def assert_close(C: torch.Tensor, C64: np.ndarray, dtype: str, algo: str, rows=N
     bound = MAXERR_SIGMA_OVERRIDE.get((algo, dtype), MAXERR_SIGMA)
     assert maxerr <= bound * sigma, f"max error {maxerr:.3e} > {bound} * sigma_C ({sigma:.3e})"
     return normwise, maxerr, sigma
+
+
+# ---------------------------------------------------------------- fused epilogue
+
+# GELU's derivative x phi(x) + Phi(x) peaks at 1.129 (x = sqrt 2): an error e in the
+# pre-activation value moves GELU by at most 1.13 e; ReLU and the identity by at most e.
+ACT_LIPSCHITZ = 1.13
+# Absolute error of the hardware tanh approximation used by GELU_TANH: below 2^-10 over the
+# whole range (the library header's stated bound); it moves x/2 (1 + tanh) by |x| 2^-11.
+TANH_HW_ABS = 2.0 ** -10
+
+
+def ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of ``dtype`` values at |x| (FP16: 11-bit significand, BF16: 8; subnormals included)."""
+    p, emin = (11, -14) if dtype == "f16" else (8, -126)
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return 2.0 ** (np.maximum(e, emin) - (p - 1))
+
+
+def padded(M: int, N: int, dtype: str, fill=None, device="cuda") -> torch.Tensor:
+    """An M x N view with rows padded to a multiple of 8 elements (16-byte row starts)."""
+    t = torch.zeros((M, (N + 7) // 8 * 8), dtype=synthetic.DTYPES[dtype], device=device)[:, :N]
+    if fill is not None:
+        t.copy_(fill)
+    return t
+
+
+def oracle_epilogue(A, B, dtype: str, bias=None, residual=None, act="none", rows=None, with_product=False):
+    """(D64, pre64[, C64]): the oracle's FP64 D = act(A.B + bias) + residual, its pre-activation
+    A.B + bias and (with_product) the product A.B itself."""
+    dt = dt_code(dtype)
+    C64 = oracle_c64(A, B, dtype, rows=rows)
+    b = None if bias is None else oracle.decode(synthetic.bits(bias), dt)
+    R = None
+    if residual is not None:
+        Rh = residual.detach().cpu()
+        if rows is not None:
+            Rh = Rh[torch.as_tensor(rows)]
+        R = oracle.decode(synthetic.bits(Rh), dt)
+    pre = C64 if b is None else C64 + b[None, :]
+    D64 = oracle.epilogue.apply(C64, b, R, act)
+    return (D64, pre, C64) if with_product else (D64, pre)
+
+
+def assert_epilogue_close(C, D64, pre64, dtype: str, act: str, gemm_err: float = 0.0, rows=None):
+    """Elementwise |C - D64| <= ACT_LIPSCHITZ * gemm_err + ulp(D) (+ the hardware tanh term).
+
+    ``gemm_err`` bounds the error of the FP32 product itself (0 where it is exact)."""
+    got = gpu_values(C, rows)
+    assert np.isfinite(got).all(), "non-finite output"
+    tol = ACT_LIPSCHITZ * gemm_err + ulp(np.maximum(np.abs(got), np.abs(D64)), dtype)
+    if act == "gelu_tanh":
+        tol = tol + 0.5 * np.abs(pre64) * TANH_HW_ABS
+    bad = np.abs(got - D64) > tol
+    assert not bad.any(), (f"{bad.sum()} elements off, worst at {np.unravel_index(np.argmax(np.abs(got - D64) - tol), got.shape)}: "
+                           f"got {got[bad][0]} want {D64[bad][0]} (tol {tol[bad][0]:.3e})")

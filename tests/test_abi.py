@@ -66,3 +66,30 @@ def test_product_path_does_not_touch_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in text.lower(), fn
+
+
+def test_epilogue_struct_layout_matches_header(tmp_path):
+    """The binding's ctypes mirror of lcgemm_epilogue has the C compiler's size and offsets."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "lcgemm.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu\\n", sizeof(lcgemm_epilogue),'
+                   ' offsetof(lcgemm_epilogue, bias), offsetof(lcgemm_epilogue, residual),'
+                   ' offsetof(lcgemm_epilogue, ldr), offsetof(lcgemm_epilogue, act)); return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    E = lcg.Epilogue
+    assert got == [ctypes.sizeof(E), E.bias.offset, E.residual.offset, E.ldr.offset, E.act.offset]
+
+
+def test_epilogue_entry_rejects_planning_and_null_handles(library):
+    ep = lcg.Epilogue(None, None, 0, lcg.ACT_RELU)
+    assert library.lcgemm_run_epilogue(None, 8, 8, 8, None, 8, None, 8, None, 8, 1, 0, ctypes.byref(ep),
+                                       None) == lcg.ERR_ARG
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    assert h.run_epilogue_raw(8, 8, 8, None, 8, None, 8, None, 8, lcg.BF16, lcg.PLAIN, act="relu") == lcg.ERR_ARG
+    h.close()
