@@ -84,7 +84,8 @@ def _peaks():
 def _kernel_source_hash(name: str) -> str:
     path = os.path.join(ROOT, "complexity_matmul_gb300", "csrc", name)
     h = hashlib.sha256()
-    for p in sorted([path, os.path.join(ROOT, "complexity_matmul_gb300", "csrc", "ptx.cuh")]):
+    csrc = os.path.join(ROOT, "complexity_matmul_gb300", "csrc")
+    for p in sorted([path, os.path.join(csrc, "ptx.cuh"), os.path.join(csrc, "epilogue.cuh")]):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -509,6 +510,60 @@ def run_skinny(args):
                           "algo": lcg.ALGO_NAMES[h.last_algo()]}), flush=True)
 
 
+EPILOGUE_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (8192, 28672, 8192), (16, 14336, 4096),
+                   (128, 14336, 4096)]
+
+
+def run_epilogue(args):
+    """Cost of the fused epilogue C = gelu_tanh(A.B + bias) + residual against the bare GEMM, and
+    against the same epilogue as a separate element-wise pass over C (torch ops, for context)."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    dev = torch.device("cuda", 0)
+    h = lcg.Handle(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    _, _, hbm, _ = _peaks()
+    for (M, N, K) in EPILOGUE_SHAPES:
+        A, B = synthetic.operands(M, N, K, "normal", 5, "bf16", str(dev), scale_a=K ** -0.5)
+        bias = synthetic.matrix(1, N, "normal", 3005, "bf16", str(dev))[0]
+        R = synthetic.matrix(M, N, "normal", 4005, "bf16", str(dev))
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def timed(fn):
+            for _ in range(2):
+                fn()
+            ts = []
+            for _ in range(args.grid_reps):
+                flush.fill_(1.0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+            return sorted(ts)[len(ts) // 2]
+
+        t_gemm = timed(lambda: h.run(A, B, C, algo="plain"))
+        t_fused = timed(lambda: h.run(A, B, C, algo="plain", bias=bias, residual=R, act="gelu_tanh"))
+        t_sep = timed(lambda: torch.add(torch.nn.functional.gelu(h.run(A, B, C, algo="plain") + bias,
+                                                                 approximate="tanh"), R))
+        print(json.dumps({"M": M, "N": N, "K": K, "epilogue": "bias+gelu_tanh+residual",
+                          "gemm_us": round(t_gemm * 1e6, 1), "fused_us": round(t_fused * 1e6, 1),
+                          "separate_pass_us": round(t_sep * 1e6, 1),
+                          "fused_overhead": round(t_fused / t_gemm - 1.0, 4),
+                          "fused_tflops": round(2.0 * M * N * K / t_fused / 1e12, 1),
+                          "extra_bytes_min": 2 * M * N + 2 * N,
+                          "extra_bytes_min_at_hbm_us": round((2 * M * N + 2 * N) / (hbm * 1e9) * 1e6, 1)}),
+              flush=True)
+        del A, B, R, C
+    rc = h.sync_status()
+    h.close()
+    if rc:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -527,6 +582,8 @@ def main():
     ap.add_argument("--grid-out", default=None, help="--grid: write per-shape results to this JSON file")
     ap.add_argument("--grid-reps", type=int, default=5, help="--grid/--skinny: timed launches per algorithm")
     ap.add_argument("--skinny", action="store_true", help="time the LLM-shaped skinny GEMMs")
+    ap.add_argument("--epilogue", action="store_true",
+                    help="time the fused bias + GELU + residual epilogue against the bare GEMM")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -536,6 +593,8 @@ def main():
         run_grid(args)
     elif args.skinny:
         run_skinny(args)
+    elif args.epilogue:
+        run_epilogue(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

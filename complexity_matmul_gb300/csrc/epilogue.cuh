@@ -14,7 +14,8 @@
 // over C.
 //
 // GELU_TANH evaluates tanh with the hardware approximation (tanh.approx.f32),
-// the fast tanh the DeepGEMM blog uses; GELU calls CUDA's erfcf.
+// the fast tanh the DeepGEMM blog uses; GELU uses a published erfc
+// approximation (gelu_erf below).
 #pragma once
 
 #include <cstdint>
@@ -31,11 +32,27 @@ __device__ __forceinline__ float tanh_hw(float x) {
   return y;
 }
 
+// x Phi(x) with Phi(x) = erfc(-x / sqrt 2) / 2.  erfc(z) for z >= 0 is the
+// rational-times-Gaussian approximation of Abramowitz and Stegun, Handbook of
+// Mathematical Functions, formula 7.1.26 (absolute error at most 1.5e-7):
+//   erfc(z) ~ t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),  t = 1 / (1 + p z),
+// and erfc(-z) = 2 - erfc(z).  The GELU's absolute error is then below
+// 1e-7 |x| (as for the usual FP32 evaluation through erf), at two special-function
+// unit operations per element instead of a full erfc.
+__device__ __forceinline__ float gelu_erf(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  const float e = poly * t * __expf(-z * z);   // erfc(|x| / sqrt 2)
+  return x * (x >= 0.f ? fmaf(-0.5f, e, 1.f) : 0.5f * e);
+}
+
 __device__ __forceinline__ float activate(float x, int act) {
   if (act == kActRelu) return x > 0.f ? x : 0.f;
-  // x Phi(x) = x/2 erfc(-x / sqrt 2): erfc keeps its relative accuracy in the
-  // negative tail, where 1 + erf(x / sqrt 2) would cancel
-  if (act == kActGelu) return 0.5f * x * erfcf(-x * 0.70710678118654752f);
+  if (act == kActGelu) return gelu_erf(x);
   if (act == kActGeluTanh) {
     // sqrt(2/pi) * (x + 0.044715 x^3)
     const float u = 0.79788456080286536f * fmaf(0.044715f * x, x * x, x);
@@ -92,24 +109,84 @@ __device__ __forceinline__ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// The bias and residual words of one run, loaded ahead of the run's epilogue
+// so that their latency overlaps other work (the previous run's epilogue, the
+// tensor-memory load, the partial sums of a split).  Only whole, 16-byte
+// aligned runs are preloaded; store_run() loads anything else itself.
+template <int W>
+struct EpiLoads {
+  static constexpr int kVec = W >= 8 ? W / 8 : 1;
+  uint4 b[kVec];
+  uint4 r[kVec];
+  bool vb, vr;
+};
+
+template <int W>
+__device__ __forceinline__ void epilogue_load(const Epilogue& e, int64_t row, int64_t col, int n, EpiLoads<W>& L) {
+  L.vb = L.vr = false;
+  if (!e.on || n != W) return;
+  if (e.bias && aligned16(e.bias + col)) {
+    L.vb = true;
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) L.b[q] = __ldg(reinterpret_cast<const uint4*>(e.bias + col) + q);
+  }
+  const uint16_t* rp = e.residual ? e.residual + row * e.ldr + col : nullptr;
+  if (rp && aligned16(rp)) {
+    L.vr = true;
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) L.r[q] = __ldcs(reinterpret_cast<const uint4*>(rp) + q);
+  }
+}
+
+template <bool BF16, int W>
+__device__ __forceinline__ void add_loaded(float (&v)[W], const uint4 (&u)[EpiLoads<W>::kVec]) {
+#pragma unroll
+  for (int q = 0; q < W / 8; ++q) {
+    const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      float lo, hi;
+      unpack2<BF16>(w[t], lo, hi);
+      v[8 * q + 2 * t] += lo;
+      v[8 * q + 2 * t + 1] += hi;
+    }
+  }
+}
+
 // Epilogue + cast + store of v[0 .. n) = C[row, col .. col + n) (n <= W; the
-// values past n are ignored).  dst points at C[row, col].
+// values past n are ignored).  dst points at C[row, col].  `pre`: this run's
+// bias / residual words if epilogue_load() fetched them, else null.
 template <bool BF16, int W>
 __device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t col, int n, float (&v)[W],
-                                          const Epilogue& e) {
+                                          const Epilogue& e, const EpiLoads<W>* pre = nullptr) {
   const bool full = n == W;
   if (e.on) {
     if (e.bias) {
-      const uint16_t* bp = e.bias + col;
-      add_run<BF16, W, true>(v, bp, n, full && aligned16(bp));
+      if (pre && pre->vb) {
+        add_loaded<BF16, W>(v, pre->b);
+      } else {
+        const uint16_t* bp = e.bias + col;
+        add_run<BF16, W, true>(v, bp, n, full && aligned16(bp));
+      }
     }
-    if (e.act) {
+    // one branch per run, then a straight loop per activation
+    if (e.act == kActRelu) {
 #pragma unroll
-      for (int j = 0; j < W; ++j) v[j] = activate(v[j], e.act);
+      for (int j = 0; j < W; ++j) v[j] = activate(v[j], kActRelu);
+    } else if (e.act == kActGelu) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) v[j] = activate(v[j], kActGelu);
+    } else if (e.act == kActGeluTanh) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) v[j] = activate(v[j], kActGeluTanh);
     }
     if (e.residual) {
-      const uint16_t* rp = e.residual + row * e.ldr + col;
-      add_run<BF16, W, false>(v, rp, n, full && aligned16(rp));
+      if (pre && pre->vr) {
+        add_loaded<BF16, W>(v, pre->r);
+      } else {
+        const uint16_t* rp = e.residual + row * e.ldr + col;
+        add_run<BF16, W, false>(v, rp, n, full && aligned16(rp));
+      }
     }
   }
   if (W % 8 == 0 && full && aligned16(dst)) {

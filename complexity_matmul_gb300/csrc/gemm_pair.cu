@@ -77,12 +77,20 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 // Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
 template <bool BF16>
 __device__ __forceinline__ void store_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
-                                            const PlainArgs& args) {
+                                            const PlainArgs& args, const EpiLoads<32>* pre = nullptr) {
   if (row >= args.M || col >= args.N) return;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep);
+  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
+}
+
+// Issues the bias / residual loads of the 32-column chunk at (row, col), if it lies in C.
+__device__ __forceinline__ void load_chunk(int row, int col, const PlainArgs& args, EpiLoads<32>& pre) {
+  if (row < args.M && col < args.N)
+    epilogue_load<32>(args.ep, row, col, min(32, args.N - col), pre);
+  else
+    pre.vb = pre.vr = false;
 }
 
 template <bool BF16>
@@ -225,18 +233,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       pair_item(w, args, num_kb, tile, kb0, kb1, half);
       int mb, nb;
       tile_coords(tile, args, mb, nb);
+      const int row = mb * 2 * kBM + rank * kBM + q * 32 + lane;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc))) break;
       tc_fence_after();
-      const int row = mb * 2 * kBM + rank * kBM + q * 32 + lane;
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
       if (half < 0) {
+        // the next chunk's bias / residual loads are in flight while this chunk is finished
+        EpiLoads<32> pre;
+        load_chunk(row, nb * kBN, args, pre);
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + c * 32, r);
+          const EpiLoads<32> cur = pre;
+          if (c + 1 < kBN / 32) load_chunk(row, nb * kBN + (c + 1) * 32, args, pre);
           tmem_wait_ld();
-          store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args);
+          store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args, &cur);
         }
         tc_fence_before();
         __syncwarp();
@@ -275,6 +288,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < kBN / 32; ++c) {
             if (row >= args.M) break;
+            EpiLoads<32> pre;
+            load_chunk(row, nb * kBN + c * 32, args, pre);
             uint32_t r[32];
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
@@ -285,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               r[4 * v + 2] = __float_as_uint(x.z + y.z);
               r[4 * v + 3] = __float_as_uint(x.w + y.w);
             }
-            store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args);
+            store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args, &pre);
           }
         }
       }

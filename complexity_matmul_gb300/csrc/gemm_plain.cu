@@ -49,12 +49,20 @@ __device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& m
 // Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
 template <bool BF16>
 __device__ __forceinline__ void store_row_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
-                                                const PlainArgs& args) {
+                                                const PlainArgs& args, const EpiLoads<32>* pre = nullptr) {
   if (row >= args.M || col >= args.N) return;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep);
+  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
+}
+
+// Issues the bias / residual loads of the 32-column chunk at (row, col), if it lies in C.
+__device__ __forceinline__ void load_chunk(int row, int col, const PlainArgs& args, EpiLoads<32>& pre) {
+  if (row < args.M && col < args.N)
+    epilogue_load<32>(args.ep, row, col, min(32, args.N - col), pre);
+  else
+    pre.vb = pre.vr = false;
 }
 
 __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
@@ -198,19 +206,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = w / args.splits, split = w - tile * args.splits;
       int mb, nb;
       tile_coords(tile, args, mb, nb);
+      const int row = mb * kBM + q * 32 + lane;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc));
       if (!ok) break;
       tc_fence_after();
-      const int row = mb * kBM + q * 32 + lane;
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (args.splits == 1) {
+        // the next chunk's bias / residual loads are in flight while this chunk is finished
+        EpiLoads<32> pre;
+        load_chunk(row, nb * BN, args, pre);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + c * 32, r);
+          const EpiLoads<32> cur = pre;
+          if (c + 1 < BN / 32) load_chunk(row, nb * BN + (c + 1) * 32, args, pre);
           tmem_wait_ld();
-          store_row_chunk<BF16>(crow, row, nb * BN + c * 32, r, args);
+          store_row_chunk<BF16>(crow, row, nb * BN + c * 32, r, args, &cur);
         }
         tc_fence_before();
         __syncwarp();
@@ -242,15 +255,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (prev == args.splits - 1) {
           if (lane == 0) args.counters[tile * 4 + q] = 0;   // ready for the next launch
           __threadfence();
-          const float* base = args.partial + (static_cast<int64_t>(tile) * args.splits * kBM + q * 32 + lane) * BN;
+          // The quarter's valid rows x column chunks are spread over all 32 lanes,
+          // rows first, so that a skinny tile (a few valid rows) still keeps the
+          // whole warp busy; every unit sums the chunks' partials in chunk order.
+          const int rows_q = min(32, args.M - (mb * kBM + q * 32));
+          const int chunks = min(BN / 32, (args.N - nb * BN + 31) / 32);
+          const int units = rows_q > 0 ? rows_q * chunks : 0;
+          const float* qbase = args.partial + (static_cast<int64_t>(tile) * args.splits * kBM + q * 32) * BN;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            if (row >= args.M) break;
+          for (int u = lane; u < units; u += 32) {
+            const int rl = u % rows_q, c = u / rows_q;
+            const int urow = mb * kBM + q * 32 + rl;
+            EpiLoads<32> pre;
+            load_chunk(urow, nb * BN + c * 32, args, pre);
             float acc32[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc32[j] = 0.f;
             for (int sp = 0; sp < args.splits; ++sp) {
-              const float4* src = reinterpret_cast<const float4*>(base + static_cast<int64_t>(sp) * kBM * BN + c * 32);
+              const float4* src =
+                  reinterpret_cast<const float4*>(qbase + (static_cast<int64_t>(sp) * kBM + rl) * BN + c * 32);
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
                 const float4 x = __ldcg(src + v);
@@ -263,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc32[j]);
-            store_row_chunk<BF16>(crow, row, nb * BN + c * 32, r, args);
+            store_row_chunk<BF16>(Cp + static_cast<int64_t>(urow) * args.ldc, urow, nb * BN + c * 32, r, args, &pre);
           }
         }
       }

@@ -148,7 +148,9 @@ LCGEMM_API int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K,
 enum {
   LCGEMM_ACT_NONE = 0,
   LCGEMM_ACT_RELU = 1,       /* x > 0 ? x : +0                                             */
-  LCGEMM_ACT_GELU = 2,       /* x * Phi(x) = x/2 (1 + erf(x / sqrt 2))                     */
+  LCGEMM_ACT_GELU = 2,       /* x * Phi(x) = x/2 (1 + erf(x / sqrt 2)); Phi from the
+                                Abramowitz-Stegun 7.1.26 erfc form (absolute error of the
+                                result below 1e-7 |x|)                                     */
   LCGEMM_ACT_GELU_TANH = 3   /* x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), hardware
                                 tanh approximation (absolute error of tanh below 2^-10)   */
 };

@@ -97,10 +97,10 @@ def test_plain_gelu_exact_product(h, M, N, K, dtype, act):
     assert (np.abs(pre) < 2).mean() > 0.4
     assert_epilogue_close(C, D64, pre, dtype, act)
     if act == "gelu":
-        # FP32 evaluation through erfc: nearly every element is the correctly rounded value itself
+        # relative error ~1e-6 where |x| < 3: nearly every element is the correctly rounded value itself
         dt = 0 if dtype == "f16" else 1
         ref = oracle.decode(oracle.reference_output(D64, dt), dt)
-        assert (C.cpu().double().numpy() == ref).mean() > 0.97
+        assert (C.cpu().double().numpy() == ref).mean() > 0.95
 
 
 # ---------------------------------------------------------------- N(0,1) workload, scaled product
