@@ -497,6 +497,8 @@ def run_skinny(args):
     import synthetic
     dev = torch.device("cuda", 0)
     h = lcg.Handle(0)
+    if args.plain_kernel:
+        h.set_option(lcg.OPT_PLAIN_KERNEL, args.plain_kernel)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     _, _, hbm, kind = _peaks()
     for (M, N, K) in synthetic.SKINNY:
@@ -575,7 +577,8 @@ def main():
     ap.add_argument("--case", default=None, help="profiling mode: run one shape 'n' or 'M,N,K' --reps times")
     ap.add_argument("--algo", default="auto", help="algorithm for --case")
     ap.add_argument("--reps", type=int, default=3, help="launches for --case")
-    ap.add_argument("--plain-kernel", type=int, default=0, help="--case: 1 single-CTA, 2 CTA-pair plain kernel")
+    ap.add_argument("--plain-kernel", type=int, default=0,
+                    help="--case/--skinny: 1 single-CTA, 2 CTA-pair, 3 skinny plain kernel")
     ap.add_argument("--lcma-kernel", type=int, default=0, help="--case: 1 single-CTA, 2 CTA-pair fused kernel")
     ap.add_argument("--grid", choices=["quick", "full"], default=None,
                     help="cost-model accuracy on the FP16 shape grid (100-triple subset or all 1000)")

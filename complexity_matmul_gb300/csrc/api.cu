@@ -157,18 +157,110 @@ int grid_cap(const lcgemm_ctx* h) {
   return h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms;
 }
 
-// Single-CTA 128 x 256 tiles or CTA-pair 256 x 256 tiles (see gemm_pair.cu).
-int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N) {
+// Single-CTA 128 x 256 tiles, CTA-pair 256 x 256 tiles (gemm_pair.cu) or the
+// weight-streaming skinny kernel (gemm_skinny.cu).
+int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K) {
+  const bool skinny_ok = M <= kSkinnyMaxM && (N + 127) / 128 <= (int64_t(1) << 20);
+  if (h->plain_kernel == 4 && M <= kGemvMaxM) return 4;
+  if (h->plain_kernel == 3 && skinny_ok) return 3;
+  if (h->plain_kernel == 1) return 1;
+  if (h->plain_kernel == 2) return grid_cap(h) < 2 ? 1 : 2;
+  // measured choices: one or two rows stream B best on the CUDA cores (at four
+  // the FMA work makes the tiled split-K kernel faster); up to 128 rows with
+  // few 256-column tiles and a long K (where the tiled kernel would need a deep
+  // K split), the stream-K skinny kernel
+  if (M <= 2) return 4;
+  if (skinny_ok && M <= 128 && N <= 8192 && K >= 2 * N) return 3;
   if (grid_cap(h) < 2) return 1;
-  if (h->plain_kernel == 1 || h->plain_kernel == 2) return h->plain_kernel;
   return (M > 128 && N > 128) ? 2 : 1;
+}
+
+int run_gemv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+             int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
+  GemvArgs a{};
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = N;
+  a.K = K;
+  a.ep = ep;
+  return launch_gemv(a, bf16, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+}
+
+int skinny_sub(int mp, int64_t K) {
+  if (K <= 64) return 1;
+  return mp <= 64 ? 4 : 2;
+}
+
+int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+               int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
+  SkinnyLaunch L{};
+  L.bf16 = bf16;
+  L.mp = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, L.mp)) return LCGEMM_ERR_CUDA;
+  if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, 128)) return LCGEMM_ERR_CUDA;
+  SkinnyArgs& a = L.args;
+  a.C = C;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  // K boxes per stage: longer contiguous runs of each B row per fetch, while the
+  // ring keeps at least two stages
+  L.sub = skinny_sub(L.mp, K);
+  a.nblk = static_cast<int>((N + 127) / 128);
+  a.num_kb = static_cast<int>((K + 64 * L.sub - 1) / (64 * L.sub));
+  a.total = int64_t(a.nblk) * a.num_kb;
+  const int per_cta = std::max(1, kSkinnyMinKPerCta / (64 * L.sub));
+  const int64_t want = (a.total + per_cta - 1) / per_cta;
+  L.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid_cap(h), want)));
+  int rc = ensure_workspace(h, static_cast<size_t>(L.grid) * 2 * L.mp * 128 * sizeof(float), st);
+  if (rc) return rc;
+  a.partial = static_cast<float*>(h->ws);
+  // arrival counters: zeroed once when (re)allocated; the epoch tag retires old arrivals
+  const size_t nctr = static_cast<size_t>(a.nblk) * 4;
+  if (nctr > h->skinny_ctr_n) {
+    if (h->skinny_ctr) {
+      cudaStreamSynchronize(st);
+      cudaFree(h->skinny_ctr);
+      h->skinny_ctr = nullptr;
+      h->skinny_ctr_n = 0;
+    }
+    if (cudaMalloc(&h->skinny_ctr, nctr * sizeof(unsigned long long)) != cudaSuccess) {
+      h->skinny_ctr = nullptr;
+      cudaGetLastError();
+      return LCGEMM_ERR_NOMEM;
+    }
+    if (cudaMemsetAsync(h->skinny_ctr, 0, nctr * sizeof(unsigned long long), st) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+    h->skinny_ctr_n = nctr;
+    h->epoch = 0;
+  }
+  if (++h->epoch == 0) {   // 2^32 launches: start the tags over from zeroed counters
+    if (cudaMemsetAsync(h->skinny_ctr, 0, h->skinny_ctr_n * sizeof(unsigned long long), st) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+    h->epoch = 1;
+  }
+  a.counters = h->skinny_ctr;
+  a.epoch = h->epoch;
+  a.err = h->err_dev;
+  a.timeout_ns = h->timeout_ns;
+  a.ep = ep;
+  return launch_skinny(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
 }
 
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
+  const int variant = plain_variant(h, M, N, K);
+  if (variant == 4) return run_gemv(M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
+  if (variant == 3) return run_skinny(h, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
   PlainLaunch L{};
   L.bf16 = bf16;
-  const bool pair = plain_variant(h, M, N) == 2;
+  const bool pair = variant == 2;
   const int bm = pair ? 2 * kPlainBM : kPlainBM;
   L.bn = pair ? 256 : (N <= 128 ? 128 : 256);
   if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, kPlainBM)) return LCGEMM_ERR_CUDA;
@@ -302,6 +394,7 @@ int lcgemm_destroy(lcgemm_t h) {
   cudaDeviceSynchronize();
   if (h->ws) cudaFree(h->ws);
   if (h->stage) cudaFree(h->stage);
+  if (h->skinny_ctr) cudaFree(h->skinny_ctr);
   for (int i = 0; i < lcgemm_ctx::kHostEvents; ++i)
     if (h->ev[i]) cudaEventDestroy(h->ev[i]);
   if (h->copy_in) cudaStreamDestroy(h->copy_in);
@@ -516,7 +609,7 @@ int lcgemm_set_option(lcgemm_t h, int option, int64_t value) {
       h->debug_drop = static_cast<int>(value);
       return LCGEMM_OK;
     case LCGEMM_OPT_PLAIN_KERNEL:
-      if (value < 0 || value > 2) return LCGEMM_ERR_ARG;
+      if (value < 0 || value > 4) return LCGEMM_ERR_ARG;
       h->plain_kernel = static_cast<int>(value);
       return LCGEMM_OK;
     case LCGEMM_OPT_LCMA_KERNEL:

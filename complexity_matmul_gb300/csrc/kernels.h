@@ -63,6 +63,54 @@ cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream);
 // CTA-pair variant: 256 x 256 tiles per cluster of two; tensor maps use 128-row boxes for A and B.
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 
+// Skinny GEMM (M <= 256): C^T = B . A^T with 128-row blocks of B as the MMA's
+// M = 128 operand and all of A (rows padded to mp) as its N operand; the
+// (block, 64-deep K slab) iteration space is split into equal contiguous
+// ranges, one per CTA.  A block spread over several CTAs is finished by the
+// last one to arrive (per block and 32-row quarter: a counter whose high word
+// is the launch's epoch, so no reset is needed); it sums the FP32 partials of
+// the block's CTAs in K order.
+struct SkinnyArgs {
+  void* C;
+  int64_t ldc;
+  int M, N, K;
+  int nblk, num_kb;                // 128-row blocks of B, K slabs of 64 * sub
+  int64_t total;                   // nblk * num_kb
+  float* partial;                  // [grid][2][mp][128]
+  unsigned long long* counters;    // [nblk][4], (epoch << 32) | arrivals
+  unsigned int epoch;
+  int* err;
+  uint64_t timeout_ns;
+  Epilogue ep;
+};
+
+struct SkinnyLaunch {
+  CUtensorMap tmA, tmB;            // A: box mp x 64; B: box 128 x 64
+  SkinnyArgs args;
+  int mp;                          // 16, 32, 64, 128 or 256
+  int sub;                         // 64-deep K boxes per pipeline stage: 1, 2 or 4
+  bool bf16;
+  int grid;
+};
+cudaError_t launch_skinny(const SkinnyLaunch& L, cudaStream_t stream);
+constexpr int kSkinnyMaxM = 256;
+constexpr int kSkinnyMinKPerCta = 512;     // grid = min(SMs, ceil(K iterations / 512 deep))
+
+// GEMV-shaped products (M <= 4) on the CUDA cores (gemv.cu).
+struct GemvArgs {
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;
+  int64_t ldc;
+  int M;
+  int64_t N, K;
+  Epilogue ep;
+};
+constexpr int kGemvMaxM = 4;
+cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st);
+
 // ---------------------------------------------------------------- LCMA pre-pass / recombination
 
 // One operand side of the Combine-A/B pre-pass.  The raw operand is stored as

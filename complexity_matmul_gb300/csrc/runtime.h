@@ -16,13 +16,17 @@ struct lcgemm_ctx {
   int split = 1;
   int max_ctas = 0;
   int debug_drop = 0;
-  int plain_kernel = 0;         // 0: choose, 1: single-CTA 128 x 256 tiles, 2: CTA-pair 256 x 256 tiles
+  int plain_kernel = 0;         // 0: choose, 1: single-CTA 128 x 256 tiles, 2: CTA-pair 256 x 256 tiles,
+                                // 3: skinny (M <= 256; larger M choose), 4: CUDA-core GEMV (M <= 4)
   int lcma_kernel = 0;          // fused one-level: 0 choose, 1 single-CTA 128 x 128 Groups, 2 CTA-pair 256 x 128
   double peak_gflops = 2.25e6;  // dense FP16/BF16 tensor peak (GFLOP/s)
   double hbm_gbps = 8000.0;     // HBM bandwidth (GB/s)
   int last_algo = -1;
   void* ws = nullptr;           // Strassen workspace (summed operands, partials, flags)
   size_t ws_bytes = 0;
+  unsigned long long* skinny_ctr = nullptr;   // skinny kernel's epoch-tagged arrival counters
+  size_t skinny_ctr_n = 0;
+  unsigned int epoch = 0;       // per skinny launch; counters of older epochs read as zero
   void* stage = nullptr;        // staging for lcgemm_run_host
   size_t stage_bytes = 0;
   // lcgemm_run_host pipeline: copy streams (host->device, device->host) and events

@@ -15,12 +15,13 @@ from helpers import (MAXERR_SIGMA, assert_bit_exact, assert_epilogue_close, orac
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["single_cta", "cta_pair"])
+@pytest.fixture(scope="module", params=[1, 2, 3, 4], ids=["single_cta", "cta_pair", "skinny", "gemv"])
 def h(request):
-    """Plain tests run on both plain kernels, Strassen tests on both fused one-level kernels."""
+    """Plain tests run on each plain kernel (3: the skinny kernel where M <= 256, 4: the GEMV where
+    M <= 4), Strassen tests on both fused one-level kernels."""
     handle = lcg.Handle(0)
     handle.set_option(lcg.OPT_PLAIN_KERNEL, request.param)
-    handle.set_option(lcg.OPT_LCMA_KERNEL, request.param)
+    handle.set_option(lcg.OPT_LCMA_KERNEL, min(request.param, 2))
     yield handle
     handle.close()
 

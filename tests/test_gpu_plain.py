@@ -12,9 +12,10 @@ from helpers import assert_bit_exact, assert_close, oracle_c64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["single_cta", "cta_pair"])
+@pytest.fixture(scope="module", params=[1, 2, 3, 4], ids=["single_cta", "cta_pair", "skinny", "gemv"])
 def h(request):
-    """Every plain test runs on both kernels: single-CTA 128x256 tiles and CTA-pair 256x256 tiles."""
+    """Every plain test runs on each kernel: single-CTA 128x256 tiles, CTA-pair 256x256 tiles, the
+    stream-K skinny kernel (M <= 256) and the CUDA-core GEMV (M <= 4); other M choose."""
     handle = lcg.Handle(0)
     handle.set_option(lcg.OPT_PLAIN_KERNEL, request.param)
     yield handle
