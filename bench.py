@@ -429,6 +429,11 @@ def run_case(args):
         sys.exit(1)
 
 
+# A device-side sleep (~0.2 ms) between the L2 flush and the timed launch: the host enqueues the
+# launch while the GPU sleeps, so no host-side gap lands between the two events of a short kernel.
+HOST_COVER_CYCLES = 400_000
+
+
 def _time_launch(h, A, B, C, algo, reps, flush):
     """Median device time (s) of `reps` launches, L2 flushed before each."""
     import torch
@@ -437,6 +442,7 @@ def _time_launch(h, A, B, C, algo, reps, flush):
     ts = []
     for _ in range(reps):
         flush.fill_(1.0)
+        torch.cuda._sleep(HOST_COVER_CYCLES)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         h.run(A, B, C, algo=algo)
@@ -539,6 +545,7 @@ def run_epilogue(args):
             ts = []
             for _ in range(args.grid_reps):
                 flush.fill_(1.0)
+                torch.cuda._sleep(HOST_COVER_CYCLES)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 fn()
