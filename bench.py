@@ -417,6 +417,8 @@ def run_case(args):
         h.set_option(lcg.OPT_PLAIN_KERNEL, args.plain_kernel)
     if args.lcma_kernel:
         h.set_option(lcg.OPT_LCMA_KERNEL, args.lcma_kernel)
+    if args.group_order is not None:
+        h.set_option(lcg.OPT_GROUP_ORDER, args.group_order)
     A, B = synthetic.operands(M, N, K, "normal", 2, "bf16", str(dev))
     C = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :N]
     for _ in range(args.reps):
@@ -518,6 +520,43 @@ def run_skinny(args):
                           "algo": lcg.ALGO_NAMES[h.last_algo()]}), flush=True)
 
 
+def run_large(args):
+    """The large rectangular BF16 shapes: plain, one- and two-level Strassen, and the one-level fused
+    kernel with Group ordering off and the tail split off; effective and actual-MMA TFLOP/s, with the
+    SM clock sampled during each variant's launches."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    variants = [("plain", "plain", {}), ("strassen1", "strassen1", {}), ("strassen2", "strassen2", {}),
+                ("strassen1 order off", "strassen1", {lcg.OPT_GROUP_ORDER: 0}),
+                ("strassen1 split off", "strassen1", {lcg.OPT_SPLIT: 0})]
+    mma_frac = {"plain": 1.0, "strassen1": 7 / 8, "strassen2": 49 / 64}
+    for (M, N, K) in synthetic.LARGE_RECT:
+        A, B = synthetic.operands(M, N, K, "normal", 5, "bf16", str(dev))
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        out = {}
+        for name, algo, opts in variants:
+            h = lcg.Handle(0)
+            for k, v in opts.items():
+                h.set_option(k, v)
+            with ClockSampler(0) as clk:
+                t = _time_launch(h, A, B, C, algo, args.grid_reps, flush)
+            rc = h.sync_status()
+            h.close()
+            if rc:
+                raise RuntimeError(f"device status {rc} for {name}")
+            eff = 2.0 * M * N * K / t / 1e12
+            cs = clk.summary()
+            out[name] = {"ms": round(t * 1e3, 3), "eff_tflops": round(eff, 1),
+                         "mma_tflops": round(eff * mma_frac[algo], 1), "sm_mhz": cs.get("sm_mhz"),
+                         "reasons": cs.get("reasons")}
+        print(json.dumps({"M": M, "N": N, "K": K, **out}), flush=True)
+        del A, B, C
+
+
 EPILOGUE_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (8192, 28672, 8192), (16, 14336, 4096),
                    (128, 14336, 4096)]
 
@@ -592,6 +631,9 @@ def main():
     ap.add_argument("--grid-out", default=None, help="--grid: write per-shape results to this JSON file")
     ap.add_argument("--grid-reps", type=int, default=5, help="--grid/--skinny: timed launches per algorithm")
     ap.add_argument("--skinny", action="store_true", help="time the LLM-shaped skinny GEMMs")
+    ap.add_argument("--large", action="store_true",
+                    help="large rectangular shapes: plain, Strassen and its ordering / split ablations")
+    ap.add_argument("--group-order", type=int, default=None, help="--case: Strassen Group ordering 0/1")
     ap.add_argument("--epilogue", action="store_true",
                     help="time the fused bias + GELU + residual epilogue against the bare GEMM")
     args = ap.parse_args()
@@ -605,6 +647,8 @@ def main():
         run_skinny(args)
     elif args.epilogue:
         run_epilogue(args)
+    elif args.large:
+        run_large(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
