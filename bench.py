@@ -557,6 +557,38 @@ def run_large(args):
         del A, B, C
 
 
+PADDED_SHAPES = [((8191, 8193, 8190), (8192, 8192, 8192)), ((16383, 16385, 8191), (16384, 16384, 8192))]
+
+
+def run_padded(args):
+    """Strassen on shapes its block split cannot divide (zero-padded operand copies) against the
+    neighbouring divisible shape, and plain on both."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    dev = torch.device("cuda", 0)
+    h = lcg.Handle(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for odd, even in PADDED_SHAPES:
+        row = {}
+        for tag, (M, N, K) in (("odd", odd), ("even", even)):
+            A, B = synthetic.operands(M, N, K, "normal", 5, "bf16", str(dev))
+            A = torch.zeros((M, (K + 7) // 8 * 8), dtype=A.dtype, device=dev)[:, :K].copy_(A)
+            B = torch.zeros((N, (K + 7) // 8 * 8), dtype=B.dtype, device=dev)[:, :K].copy_(B)
+            C = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :N]
+            for algo in ("plain", "strassen1", "strassen2"):
+                t = _time_launch(h, A, B, C, algo, args.grid_reps, flush)
+                row[f"{tag} {algo}"] = {"shape": [M, N, K], "ms": round(t * 1e3, 3),
+                                        "eff_tflops": round(2.0 * M * N * K / t / 1e12, 1)}
+            del A, B, C
+        print(json.dumps(row), flush=True)
+    rc = h.sync_status()
+    h.close()
+    if rc:
+        sys.exit(1)
+
+
 EPILOGUE_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (8192, 28672, 8192), (16, 14336, 4096),
                    (128, 14336, 4096)]
 
@@ -634,6 +666,8 @@ def main():
     ap.add_argument("--large", action="store_true",
                     help="large rectangular shapes: plain, Strassen and its ordering / split ablations")
     ap.add_argument("--group-order", type=int, default=None, help="--case: Strassen Group ordering 0/1")
+    ap.add_argument("--padded", action="store_true",
+                    help="Strassen on non-divisible shapes (zero-padded operands) against divisible ones")
     ap.add_argument("--epilogue", action="store_true",
                     help="time the fused bias + GELU + residual epilogue against the bare GEMM")
     args = ap.parse_args()
@@ -649,6 +683,8 @@ def main():
         run_epilogue(args)
     elif args.large:
         run_large(args)
+    elif args.padded:
+        run_padded(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -395,6 +395,7 @@ int lcgemm_destroy(lcgemm_t h) {
   if (h->ws) cudaFree(h->ws);
   if (h->stage) cudaFree(h->stage);
   if (h->skinny_ctr) cudaFree(h->skinny_ctr);
+  if (h->pad) cudaFree(h->pad);
   for (int i = 0; i < lcgemm_ctx::kHostEvents; ++i)
     if (h->ev[i]) cudaEventDestroy(h->ev[i]);
   if (h->copy_in) cudaStreamDestroy(h->copy_in);

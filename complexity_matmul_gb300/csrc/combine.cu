@@ -128,9 +128,12 @@ __global__ void __launch_bounds__(256) combine_h_kernel(const __grid_constant__ 
           acc[3] += w * m.w;
         }
         const int64_t row = br * int64_t(a.mb) + i;
+        const int64_t gcol = bc * int64_t(a.nb) + j;
+        if (row >= a.M || gcol >= a.N) continue;
         uint16_t* crow = a.C + row * a.ldc + bc * int64_t(a.nb);
-        const int n = static_cast<int>(a.nb - j < 4 ? a.nb - j : 4);
-        store_run<BF16, 4>(crow + j, row, bc * int64_t(a.nb) + j, n, acc, a.ep);
+        int n = static_cast<int>(a.nb - j < 4 ? a.nb - j : 4);
+        if (a.N - gcol < n) n = static_cast<int>(a.N - gcol);
+        store_run<BF16, 4>(crow + j, row, gcol, n, acc, a.ep);
       }
   }
 }

@@ -139,6 +139,7 @@ struct CombineHArgs {
   int64_t ldc;
   int mb, nb;
   Epilogue ep;          // applied in C's coordinates
+  int M, N;             // C's extents: blocks of zero-padded operands may reach past them
 };
 cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st);
 
@@ -170,6 +171,7 @@ struct LcmaArgs {
   int* err;
   uint64_t timeout_ns;
   Epilogue ep;                    // applied in C's coordinates when a value is final
+  int M, N;                       // C's extents: blocks of zero-padded operands may reach past them
 };
 
 struct LcmaLaunch {

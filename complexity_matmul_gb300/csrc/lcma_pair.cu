@@ -271,8 +271,9 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
         const int64_t crow_i = static_cast<int64_t>(qr) * a.mb + rloc;
         uint16_t* crow = Cp + crow_i * a.ldc + static_cast<int64_t>(qc) * a.nb;
         const int qcol = tile_col0 + col;              // column inside the quadrant
-        if (rloc < a.mb && qcol < a.nb)
-          store_run<BF16, 32>(crow + qcol, crow_i, static_cast<int64_t>(qc) * a.nb + qcol, min(32, a.nb - qcol), v,
+        const int64_t gcol = static_cast<int64_t>(qc) * a.nb + qcol;
+        if (rloc < a.mb && qcol < a.nb && crow_i < a.M && gcol < a.N)
+          store_run<BF16, 32>(crow + qcol, crow_i, gcol, min(min(32, a.nb - qcol), static_cast<int>(a.N - gcol)), v,
                               a.ep);
       }
     }

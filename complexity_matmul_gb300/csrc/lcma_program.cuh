@@ -170,11 +170,13 @@ __device__ __forceinline__ void store_quadrant(uint32_t tsrc, const LcmaArgs& a,
     tmem_ld_32x32b_x32(tsrc + c * 32, r);
     tmem_wait_ld();
     const int col = col0 + c * 32;
-    if (rloc < a.mb && col < a.nb) {
+    const int64_t gcol = static_cast<int64_t>(qc) * a.nb + col;
+    if (rloc < a.mb && col < a.nb && row < a.M && gcol < a.N) {
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      store_run<BF16, 32>(crow + col, row, static_cast<int64_t>(qc) * a.nb + col, min(32, a.nb - col), v, a.ep);
+      const int n = min(min(32, a.nb - col), static_cast<int>(a.N - gcol));
+      store_run<BF16, 32>(crow + col, row, gcol, n, v, a.ep);
     }
   }
 }

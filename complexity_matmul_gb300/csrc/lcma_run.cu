@@ -36,9 +36,12 @@ int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st) {
 
 namespace {
 
+// M, N, K: the (divisible) operand extents; Mc x Nc: C's extents (smaller when the
+// operands are zero-padded copies).
 template <int L>
 int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-               const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
+               const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st,
+               int64_t Mc, int64_t Nc) {
   constexpr LcmaPlan<L> plan{};
   constexpr int G = plan.G;
   const int64_t mb = M / G, nb = N / G, kb = K / G;
@@ -125,6 +128,8 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
   a.ep = ep;
+  a.M = static_cast<int>(Mc);
+  a.N = static_cast<int>(Nc);
   if (pair) {
     // Stream-K style split of the tail: when the last, partial wave of Groups
     // fits twice over, its Groups run as two halves on two pairs each.
@@ -148,19 +153,63 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   }
   ll.grid = std::min(a.num_groups * plan.R, grid_cap(h));
   if (launch_lcma_products(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
-  CombineHArgs ch{prod, ldp, static_cast<uint16_t*>(C), ldc, static_cast<int>(mb), static_cast<int>(nb), ep};
+  CombineHArgs ch{prod, ldp, static_cast<uint16_t*>(C), ldc, static_cast<int>(mb), static_cast<int>(nb), ep,
+                  static_cast<int>(Mc), static_cast<int>(Nc)};
   if (launch_combine_h(ch, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
   return LCGEMM_OK;
 }
 
 }  // namespace
 
+// Strassen on any shape: dimensions that the block split cannot divide (M, N by
+// 2^levels, K by 16 * 2^(levels-1)) are zero-padded -- A and B are copied into
+// zero-filled M' x K' and N' x K' buffers; the products of the padding are zero
+// and the kernels store only C's M x N elements, so C is exact up to the same
+// rounding as on a divisible shape.
 int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, int64_t K, const void* A,
                  int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep,
                  cudaStream_t st) {
-  if (levels == 1) return run_levels<1>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
-  if (levels == 2) return run_levels<2>(h, fused, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
-  return LCGEMM_ERR_UNSUPPORTED;
+  if (levels != 1 && levels != 2) return LCGEMM_ERR_UNSUPPORTED;
+  const int64_t G = int64_t(1) << levels;
+  const int64_t Mp = round_up(M, G), Np = round_up(N, G), Kp = round_up(K, 8 * G);
+  const void* Ap = A;
+  const void* Bp = B;
+  int64_t ldap = lda, ldbp = ldb;
+  if (Mp != M || Np != N || Kp != K) {
+    const int64_t a_bytes = round_up(Mp * Kp * 2, 256), b_bytes = round_up(Np * Kp * 2, 256);
+    const size_t need = static_cast<size_t>(a_bytes + b_bytes);
+    if (need > h->pad_bytes) {
+      if (h->pad) {
+        cudaStreamSynchronize(st);
+        cudaFree(h->pad);
+        h->pad = nullptr;
+        h->pad_bytes = 0;
+      }
+      if (cudaMalloc(&h->pad, need) != cudaSuccess) {
+        h->pad = nullptr;
+        cudaGetLastError();
+        return LCGEMM_ERR_NOMEM;
+      }
+      h->pad_bytes = need;
+    }
+    char* pa = static_cast<char*>(h->pad);
+    char* pb = pa + a_bytes;
+    // real part, then the padding columns of every row, then the padding rows
+    const auto pad_copy = [&](char* dst, const void* src, int64_t ld, int64_t rows, int64_t rows_p) {
+      if (cudaMemcpy2DAsync(dst, Kp * 2, src, ld * 2, K * 2, rows, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return false;
+      if (Kp > K && cudaMemset2DAsync(dst + K * 2, Kp * 2, 0, (Kp - K) * 2, rows, st) != cudaSuccess) return false;
+      if (rows_p > rows && cudaMemsetAsync(dst + rows * Kp * 2, 0, (rows_p - rows) * Kp * 2, st) != cudaSuccess)
+        return false;
+      return true;
+    };
+    if (!pad_copy(pa, A, lda, M, Mp) || !pad_copy(pb, B, ldb, N, Np)) return LCGEMM_ERR_CUDA;
+    Ap = pa;
+    Bp = pb;
+    ldap = ldbp = Kp;
+  }
+  if (levels == 1) return run_levels<1>(h, fused, Mp, Np, Kp, Ap, ldap, Bp, ldbp, C, ldc, bf16, ep, st, M, N);
+  return run_levels<2>(h, fused, Mp, Np, Kp, Ap, ldap, Bp, ldbp, C, ldc, bf16, ep, st, M, N);
 }
 
 }  // namespace lcg

@@ -141,6 +141,8 @@ extern "C" LCGEMM_API int lcgemm_strassen1_noalloc(int64_t M, int64_t N, int64_t
   a.mb = static_cast<int>(mb);
   a.nb = static_cast<int>(nb);
   a.kb = static_cast<int>(kb);
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
   a.tiles_m = static_cast<int>((mb + 127) / 128);
   a.tiles_n = static_cast<int>((nb + 127) / 128);
   a.num_groups = a.tiles_m * a.tiles_n;

@@ -26,9 +26,9 @@ bool algo_supported(int algo, int64_t M, int64_t N, int64_t K) {
       return true;
     case LCGEMM_STRASSEN1:
     case LCGEMM_STRASSEN1_UNFUSED:
-      return M >= 2 && N >= 2 && K >= 16 && M % 2 == 0 && N % 2 == 0 && K % 16 == 0;
     case LCGEMM_STRASSEN2:
-      return M >= 4 && N >= 4 && K >= 32 && M % 4 == 0 && N % 4 == 0 && K % 32 == 0;
+      // any shape: non-divisible dimensions run on zero-padded operand copies
+      return M >= 1 && N >= 1 && K >= 1;
     default:
       return false;
   }
@@ -73,6 +73,9 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
+double estimate_divisible(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, double P, double BW,
+                          int sms);
+
 double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K) {
   const double P = h->peak_gflops * 1e9;
   const double BW = h->hbm_gbps * 1e9;
@@ -96,6 +99,26 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
     return kernel_time(mnk2, bytes, cdiv(M, 128) * cdiv(N, bn), sms, kEtaPlainSingle, P, BW);
   }
   if (!algo_supported(algo, M, N, K)) return INFINITY;
+  // non-divisible shapes run on zero-padded copies: the copy (read the operands,
+  // write the padded ones) comes first, then the algorithm on the padded extents
+  const int64_t G = algo == LCGEMM_STRASSEN2 ? 4 : 2;
+  const int64_t Mp = cdiv(M, G) * G, Np = cdiv(N, G) * G, Kp = cdiv(K, 8 * G) * 8 * G;
+  double t_pad = 0.0;
+  if (Mp != M || Np != N || Kp != K) {
+    t_pad = kernel_time(0, 2.0 * (m * k + n * k) + 2.0 * static_cast<double>(Mp + Np) * static_cast<double>(Kp), 0, 1,
+                        1.0, P, BW);
+    M = Mp;
+    N = Np;
+    K = Kp;
+  }
+  return t_pad + estimate_divisible(h, algo, M, N, K, P, BW, sms);
+}
+
+// Strassen time on divisible extents.
+double estimate_divisible(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, double P, double BW,
+                          int sms) {
+  const double m = static_cast<double>(M), n = static_cast<double>(N), k = static_cast<double>(K);
+  const double mnk2 = 2.0 * m * n * k;
   if (algo == LCGEMM_STRASSEN1 || algo == LCGEMM_STRASSEN1_UNFUSED) {
     const int64_t mb = M / 2, nb = N / 2;
     // pre-pass: read A and B once, write 5 summed blocks of each (2 of 7 products alias raw blocks)

@@ -27,6 +27,8 @@ struct lcgemm_ctx {
   unsigned long long* skinny_ctr = nullptr;   // skinny kernel's epoch-tagged arrival counters
   size_t skinny_ctr_n = 0;
   unsigned int epoch = 0;       // per skinny launch; counters of older epochs read as zero
+  void* pad = nullptr;          // zero-padded operand copies for Strassen on non-divisible shapes
+  size_t pad_bytes = 0;
   void* stage = nullptr;        // staging for lcgemm_run_host
   size_t stage_bytes = 0;
   // lcgemm_run_host pipeline: copy streams (host->device, device->host) and events

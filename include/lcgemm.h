@@ -79,7 +79,8 @@ enum {
   LCGEMM_OK = 0,
   LCGEMM_ERR_ARG = -1,          /* null pointer, negative size, ld too small, bad enum    */
   LCGEMM_ERR_ALIGN = -2,        /* pointer not 16-byte aligned or ld not a multiple of 8  */
-  LCGEMM_ERR_UNSUPPORTED = -3,  /* explicit Strassen on dimensions it cannot split        */
+  LCGEMM_ERR_UNSUPPORTED = -3,  /* shape outside an entry point's range (allocation-free
+                                   entry point on dimensions it cannot split)             */
   LCGEMM_ERR_ALIAS = -4,        /* C overlaps A or B                                      */
   LCGEMM_ERR_CUDA = -5,         /* a CUDA runtime/driver call or launch failed            */
   LCGEMM_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up (earlier launch)    */
@@ -129,9 +130,11 @@ LCGEMM_API int lcgemm_destroy(lcgemm_t h);
  * C = A . B, asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy
  * default stream).  A, B, C are device pointers owned by the caller; C is
  * overwritten (beta = 0).  M = 0 or N = 0 is a no-op; K = 0 writes zeros.
- * LCGEMM_AUTO never fails with LCGEMM_ERR_UNSUPPORTED: it falls back to plain.
- * Explicit LCGEMM_STRASSEN1 needs M, N even and K a multiple of 16;
- * LCGEMM_STRASSEN2 needs M, N multiples of 4 and K a multiple of 32.
+ * Every algorithm takes any shape.  Strassen splits M and N into 2 (one level)
+ * or 4 (two levels) blocks and K into blocks of a multiple of 8; when a
+ * dimension does not divide (M, N by 2 resp. 4, K by 16 resp. 32), A and B
+ * are first copied into zero-padded buffers owned by the handle (the padding
+ * multiplies to zero) and only C's M x N elements are written.
  */
 LCGEMM_API int lcgemm_run(lcgemm_t h, int64_t M, int64_t N, int64_t K,
                const void* A, int64_t lda, const void* B, int64_t ldb,
