@@ -138,6 +138,35 @@ __global__ void __launch_bounds__(256) combine_h_kernel(const __grid_constant__ 
   }
 }
 
+// Zero-padded copy of both operands: dst row r = src row r (K values) then
+// zeros up to kp; rows >= rows_src are all zeros.  One thread per 8 elements of
+// the destination; 16-byte loads where a run of 8 lies inside the source row.
+__global__ void __launch_bounds__(256) pad_copy_kernel(const __grid_constant__ PadArgs a) {
+  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < a.vecs[0] + a.vecs[1];
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int s = v < a.vecs[0] ? 0 : 1;
+    const PadSide& p = a.side[s];
+    const int64_t w = s == 0 ? v : v - a.vecs[0];
+    const int64_t per_row = p.kp / 8;
+    const int64_t r = w / per_row;
+    const int64_t k = (w - r * per_row) * 8;
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (r < p.rows) {
+      const uint16_t* src = p.src + r * p.ld + k;
+      if (k + 8 <= p.k) {
+        out = *reinterpret_cast<const uint4*>(src);
+      } else if (k < p.k) {
+        uint16_t e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = k + i < p.k ? src[i] : uint16_t(0);
+        out = make_uint4(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16), e[4] | (uint32_t(e[5]) << 16),
+                         e[6] | (uint32_t(e[7]) << 16));
+      }
+    }
+    *reinterpret_cast<uint4*>(p.dst + r * p.kp + k) = out;
+  }
+}
+
 template <typename K, typename Args>
 cudaError_t launch_grid_stride(K kern, const Args& a, int64_t total, int num_sms, cudaStream_t st) {
   const int threads = 256;
@@ -160,6 +189,12 @@ cudaError_t launch_combine_ab(const CombineArgs& a, int levels, bool bf16, int n
     return bf16 ? launch_grid_stride(combine_ab_kernel<2, true>, a, total, num_sms, st)
                 : launch_grid_stride(combine_ab_kernel<2, false>, a, total, num_sms, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pad_copy(const PadArgs& a, int num_sms, cudaStream_t st) {
+  const int64_t total = a.vecs[0] + a.vecs[1];
+  if (total == 0) return cudaSuccess;
+  return launch_grid_stride(pad_copy_kernel, a, total, num_sms, st);
 }
 
 cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st) {

@@ -131,6 +131,20 @@ struct CombineArgs {
 };
 cudaError_t launch_combine_ab(const CombineArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st);
 
+// Zero-padded copies of A and B for Strassen on non-divisible shapes: dst is
+// rows_p x kp (row stride kp, a multiple of 8), src rows x k with stride ld.
+struct PadSide {
+  const uint16_t* src;
+  int64_t ld, rows, k;
+  uint16_t* dst;
+  int64_t rows_p, kp;
+};
+struct PadArgs {
+  PadSide side[2];
+  int64_t vecs[2];     // rows_p * kp / 8 per side
+};
+cudaError_t launch_pad_copy(const PadArgs& a, int num_sms, cudaStream_t st);
+
 // Recombination of FP32 products [R][mb][ldp] into the G x G blocks of C.
 struct CombineHArgs {
   const float* prod;

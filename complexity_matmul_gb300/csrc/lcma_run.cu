@@ -161,22 +161,24 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
 
 }  // namespace
 
-// Strassen on any shape: dimensions that the block split cannot divide (M, N by
-// 2^levels, K by 16 * 2^(levels-1)) are zero-padded -- A and B are copied into
-// zero-filled M' x K' and N' x K' buffers; the products of the padding are zero
-// and the kernels store only C's M x N elements, so C is exact up to the same
-// rounding as on a divisible shape.
+// Strassen on any shape: dimensions that the block split cannot divide (M by
+// 2^levels, K by 8 * 2^levels) -- and N unless its blocks start on 16-byte
+// boundaries (N by 8 * 2^levels), which keeps C's quadrant stores vectorised --
+// run on zero-padded copies of the operand(s) concerned.  The products of the
+// padding are zero and the kernels store only C's M x N elements, so C is exact
+// up to the same rounding as on a divisible shape.
 int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, int64_t K, const void* A,
                  int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep,
                  cudaStream_t st) {
   if (levels != 1 && levels != 2) return LCGEMM_ERR_UNSUPPORTED;
   const int64_t G = int64_t(1) << levels;
-  const int64_t Mp = round_up(M, G), Np = round_up(N, G), Kp = round_up(K, 8 * G);
+  const int64_t Mp = round_up(M, G), Np = round_up(N, 8 * G), Kp = round_up(K, 8 * G);
+  const bool pad_a = Mp != M || Kp != K, pad_b = Np != N || Kp != K;
   const void* Ap = A;
   const void* Bp = B;
   int64_t ldap = lda, ldbp = ldb;
-  if (Mp != M || Np != N || Kp != K) {
-    const int64_t a_bytes = round_up(Mp * Kp * 2, 256), b_bytes = round_up(Np * Kp * 2, 256);
+  if (pad_a || pad_b) {
+    const int64_t a_bytes = pad_a ? round_up(Mp * Kp * 2, 256) : 0, b_bytes = pad_b ? round_up(Np * Kp * 2, 256) : 0;
     const size_t need = static_cast<size_t>(a_bytes + b_bytes);
     if (need > h->pad_bytes) {
       if (h->pad) {
@@ -194,19 +196,20 @@ int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, in
     }
     char* pa = static_cast<char*>(h->pad);
     char* pb = pa + a_bytes;
-    // real part, then the padding columns of every row, then the padding rows
-    const auto pad_copy = [&](char* dst, const void* src, int64_t ld, int64_t rows, int64_t rows_p) {
-      if (cudaMemcpy2DAsync(dst, Kp * 2, src, ld * 2, K * 2, rows, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-        return false;
-      if (Kp > K && cudaMemset2DAsync(dst + K * 2, Kp * 2, 0, (Kp - K) * 2, rows, st) != cudaSuccess) return false;
-      if (rows_p > rows && cudaMemsetAsync(dst + rows * Kp * 2, 0, (rows_p - rows) * Kp * 2, st) != cudaSuccess)
-        return false;
-      return true;
-    };
-    if (!pad_copy(pa, A, lda, M, Mp) || !pad_copy(pb, B, ldb, N, Np)) return LCGEMM_ERR_CUDA;
-    Ap = pa;
-    Bp = pb;
-    ldap = ldbp = Kp;
+    PadArgs pad{};
+    if (pad_a) {
+      pad.side[0] = PadSide{static_cast<const uint16_t*>(A), lda, M, K, reinterpret_cast<uint16_t*>(pa), Mp, Kp};
+      pad.vecs[0] = Mp * Kp / 8;
+      Ap = pa;
+      ldap = Kp;
+    }
+    if (pad_b) {
+      pad.side[1] = PadSide{static_cast<const uint16_t*>(B), ldb, N, K, reinterpret_cast<uint16_t*>(pb), Np, Kp};
+      pad.vecs[1] = Np * Kp / 8;
+      Bp = pb;
+      ldbp = Kp;
+    }
+    if (launch_pad_copy(pad, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
   }
   if (levels == 1) return run_levels<1>(h, fused, Mp, Np, Kp, Ap, ldap, Bp, ldbp, C, ldc, bf16, ep, st, M, N);
   return run_levels<2>(h, fused, Mp, Np, Kp, Ap, ldap, Bp, ldbp, C, ldc, bf16, ep, st, M, N);

@@ -102,11 +102,14 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
   // non-divisible shapes run on zero-padded copies: the copy (read the operands,
   // write the padded ones) comes first, then the algorithm on the padded extents
   const int64_t G = algo == LCGEMM_STRASSEN2 ? 4 : 2;
-  const int64_t Mp = cdiv(M, G) * G, Np = cdiv(N, G) * G, Kp = cdiv(K, 8 * G) * 8 * G;
+  const int64_t Mp = cdiv(M, G) * G, Np = cdiv(N, 8 * G) * 8 * G, Kp = cdiv(K, 8 * G) * 8 * G;
+  const bool pad_a = Mp != M || Kp != K, pad_b = Np != N || Kp != K;
   double t_pad = 0.0;
-  if (Mp != M || Np != N || Kp != K) {
-    t_pad = kernel_time(0, 2.0 * (m * k + n * k) + 2.0 * static_cast<double>(Mp + Np) * static_cast<double>(Kp), 0, 1,
-                        1.0, P, BW);
+  if (pad_a || pad_b) {
+    const double kp = static_cast<double>(Kp);
+    const double bytes = (pad_a ? 2.0 * m * k + 2.0 * static_cast<double>(Mp) * kp : 0.0) +
+                         (pad_b ? 2.0 * n * k + 2.0 * static_cast<double>(Np) * kp : 0.0);
+    t_pad = kernel_time(0, bytes, 0, 1, 1.0, P, BW);
     M = Mp;
     N = Np;
     K = Kp;
