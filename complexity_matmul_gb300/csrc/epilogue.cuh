@@ -153,6 +153,30 @@ __device__ __forceinline__ void add_loaded(float (&v)[W], const uint4 (&u)[EpiLo
   }
 }
 
+// One rounding of v[0 .. n) to the output type and its store at dst (n <= W):
+// 16-byte stores for a whole, aligned run, 2-byte stores otherwise.
+template <bool BF16, int W>
+__device__ __forceinline__ void cast_store(uint16_t* dst, int n, const float (&v)[W]) {
+  if (W % 8 == 0 && n == W && aligned16(dst)) {
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+      uint4 o;
+      o.x = pack2(v[8 * q + 0], v[8 * q + 1], BF16);
+      o.y = pack2(v[8 * q + 2], v[8 * q + 3], BF16);
+      o.z = pack2(v[8 * q + 4], v[8 * q + 5], BF16);
+      o.w = pack2(v[8 * q + 6], v[8 * q + 7], BF16);
+      reinterpret_cast<uint4*>(dst)[q] = o;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; j += 2) {
+      const uint32_t p = pack2(v[j], j + 1 < W ? v[j + 1] : 0.f, BF16);
+      if (j < n) dst[j] = static_cast<uint16_t>(p & 0xffffu);
+      if (j + 1 < n) dst[j + 1] = static_cast<uint16_t>(p >> 16);
+    }
+  }
+}
+
 // Epilogue + cast + store of v[0 .. n) = C[row, col .. col + n) (n <= W; the
 // values past n are ignored).  dst points at C[row, col].  `pre`: this run's
 // bias / residual words if epilogue_load() fetched them, else null.
@@ -189,24 +213,7 @@ __device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t co
       }
     }
   }
-  if (W % 8 == 0 && full && aligned16(dst)) {
-#pragma unroll
-    for (int q = 0; q < W / 8; ++q) {
-      uint4 o;
-      o.x = pack2(v[8 * q + 0], v[8 * q + 1], BF16);
-      o.y = pack2(v[8 * q + 2], v[8 * q + 3], BF16);
-      o.z = pack2(v[8 * q + 4], v[8 * q + 5], BF16);
-      o.w = pack2(v[8 * q + 6], v[8 * q + 7], BF16);
-      reinterpret_cast<uint4*>(dst)[q] = o;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < W; j += 2) {
-      const uint32_t p = pack2(v[j], j + 1 < W ? v[j + 1] : 0.f, BF16);
-      if (j < n) dst[j] = static_cast<uint16_t>(p & 0xffffu);
-      if (j + 1 < n) dst[j + 1] = static_cast<uint16_t>(p >> 16);
-    }
-  }
+  cast_store<BF16, W>(dst, n, v);
 }
 
 }  // namespace lcg

@@ -75,14 +75,15 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 }
 
 // Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
-template <bool BF16>
+template <bool BF16, bool EPI>
 __device__ __forceinline__ void store_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
                                             const PlainArgs& args, const EpiLoads<32>* pre = nullptr) {
   if (row >= args.M || col >= args.N) return;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
+  if constexpr (EPI) store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
+  else cast_store<BF16, 32>(crow + col, min(32, args.N - col), v);
 }
 
 // Issues the bias / residual loads of the 32-column chunk at (row, col), if it lies in C.
@@ -93,7 +94,7 @@ __device__ __forceinline__ void load_chunk(int row, int col, const PlainArgs& ar
     pre.vb = pre.vr = false;
 }
 
-template <bool BF16>
+template <bool BF16, bool EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     plain_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const PlainArgs args) {
@@ -239,17 +240,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
       if (half < 0) {
-        // the next chunk's bias / residual loads are in flight while this chunk is finished
-        EpiLoads<32> pre;
-        load_chunk(row, nb * kBN, args, pre);
+        if constexpr (EPI) {
+          // the next chunk's bias / residual loads are in flight while this chunk is finished
+          EpiLoads<32> pre;
+          load_chunk(row, nb * kBN, args, pre);
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
-          const EpiLoads<32> cur = pre;
-          if (c + 1 < kBN / 32) load_chunk(row, nb * kBN + (c + 1) * 32, args, pre);
-          tmem_wait_ld();
-          store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args, &cur);
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            const EpiLoads<32> cur = pre;
+            if (c + 1 < kBN / 32) load_chunk(row, nb * kBN + (c + 1) * 32, args, pre);
+            tmem_wait_ld();
+            store_chunk<BF16, true>(crow, row, nb * kBN + c * 32, r, args, &cur);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            tmem_wait_ld();
+            store_chunk<BF16, false>(crow, row, nb * kBN + c * 32, r, args);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -289,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kBN / 32; ++c) {
             if (row >= args.M) break;
             EpiLoads<32> pre;
-            load_chunk(row, nb * kBN + c * 32, args, pre);
+            if constexpr (EPI) load_chunk(row, nb * kBN + c * 32, args, pre);
             uint32_t r[32];
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
@@ -300,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               r[4 * v + 2] = __float_as_uint(x.z + y.z);
               r[4 * v + 3] = __float_as_uint(x.w + y.w);
             }
-            store_chunk<BF16>(crow, row, nb * kBN + c * 32, r, args, &pre);
+            store_chunk<BF16, EPI>(crow, row, nb * kBN + c * 32, r, args, &pre);
           }
         }
       }
@@ -317,9 +328,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool EPI>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
-  auto kern = plain_pair_kernel<BF16>;
+  auto kern = plain_pair_kernel<BF16, EPI>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -334,7 +345,9 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream) {
   if (L.grid % 2) return cudaErrorInvalidValue;
-  return L.bf16 ? launch_impl<true>(L, stream) : launch_impl<false>(L, stream);
+  // the kernel without an epilogue keeps the lean store path
+  if (L.args.ep.on) return L.bf16 ? launch_impl<true, true>(L, stream) : launch_impl<false, true>(L, stream);
+  return L.bf16 ? launch_impl<true, false>(L, stream) : launch_impl<false, false>(L, stream);
 }
 
 }  // namespace lcg

@@ -47,14 +47,15 @@ __device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& m
 }
 
 // Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
-template <bool BF16>
+template <bool BF16, bool EPI>
 __device__ __forceinline__ void store_row_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
                                                 const PlainArgs& args, const EpiLoads<32>* pre = nullptr) {
   if (row >= args.M || col >= args.N) return;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
+  if constexpr (EPI) store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
+  else cast_store<BF16, 32>(crow + col, min(32, args.N - col), v);
 }
 
 // Issues the bias / residual loads of the 32-column chunk at (row, col), if it lies in C.
@@ -71,7 +72,7 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
   return old;
 }
 
-template <int BN, int STAGES, bool BF16>
+template <int BN, int STAGES, bool BF16, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     plain_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const PlainArgs args) {
@@ -213,17 +214,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (args.splits == 1) {
-        // the next chunk's bias / residual loads are in flight while this chunk is finished
-        EpiLoads<32> pre;
-        load_chunk(row, nb * BN, args, pre);
+        if constexpr (EPI) {
+          // the next chunk's bias / residual loads are in flight while this chunk is finished
+          EpiLoads<32> pre;
+          load_chunk(row, nb * BN, args, pre);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
-          const EpiLoads<32> cur = pre;
-          if (c + 1 < BN / 32) load_chunk(row, nb * BN + (c + 1) * 32, args, pre);
-          tmem_wait_ld();
-          store_row_chunk<BF16>(crow, row, nb * BN + c * 32, r, args, &cur);
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            const EpiLoads<32> cur = pre;
+            if (c + 1 < BN / 32) load_chunk(row, nb * BN + (c + 1) * 32, args, pre);
+            tmem_wait_ld();
+            store_row_chunk<BF16, true>(crow, row, nb * BN + c * 32, r, args, &cur);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            tmem_wait_ld();
+            store_row_chunk<BF16, false>(crow, row, nb * BN + c * 32, r, args);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -267,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rl = u % rows_q, c = u / rows_q;
             const int urow = mb * kBM + q * 32 + rl;
             EpiLoads<32> pre;
-            load_chunk(urow, nb * BN + c * 32, args, pre);
+            if constexpr (EPI) load_chunk(urow, nb * BN + c * 32, args, pre);
             float acc32[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc32[j] = 0.f;
@@ -286,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc32[j]);
-            store_row_chunk<BF16>(Cp + static_cast<int64_t>(urow) * args.ldc, urow, nb * BN + c * 32, r, args, &pre);
+            store_row_chunk<BF16, EPI>(Cp + static_cast<int64_t>(urow) * args.ldc, urow, nb * BN + c * 32, r, args,
+                                       &pre);
           }
         }
       }
@@ -303,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool BF16>
+template <int BN, int STAGES, bool BF16, bool EPI>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
-  auto kern = plain_gemm_kernel<BN, STAGES, BF16>;
+  auto kern = plain_gemm_kernel<BN, STAGES, BF16, EPI>;
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -320,8 +332,13 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream) {
-  if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true>(L, stream) : launch_impl<256, 4, false>(L, stream);
-  if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true>(L, stream) : launch_impl<128, 6, false>(L, stream);
+  // the kernel without an epilogue keeps the lean store path
+  if (L.args.ep.on) {
+    if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true, true>(L, stream) : launch_impl<256, 4, false, true>(L, stream);
+    if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true, true>(L, stream) : launch_impl<128, 6, false, true>(L, stream);
+  }
+  if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true, false>(L, stream) : launch_impl<256, 4, false, false>(L, stream);
+  if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true, false>(L, stream) : launch_impl<128, 6, false, false>(L, stream);
   return cudaErrorInvalidValue;
 }
 
