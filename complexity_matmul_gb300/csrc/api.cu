@@ -170,7 +170,7 @@ int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K) {
   // few 256-column tiles and a long K (where the tiled kernel would need a deep
   // K split), the stream-K skinny kernel
   if (M <= 2) return 4;
-  if (skinny_ok && M <= 128 && N <= 8192 && K >= 2 * N) return 3;
+  if (skinny_ok && M <= 128 && N >= 1024 && N <= 8192 && K >= 2 * N) return 3;
   if (grid_cap(h) < 2) return 1;
   return (M > 128 && N > 128) ? 2 : 1;
 }
@@ -284,11 +284,12 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   a.kb_per_split = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
   if (!pair) {
     // Too few tiles to fill the machine (skinny M, small N): cut K into chunks
-    // of at least 8 slabs so that tiles x chunks approaches the SM count.
+    // of at least 16 slabs so that tiles x chunks approaches the SM count.
     const int num_kb = a.kb_per_split;
     const int cap = grid_cap(h);
-    if (tiles < cap / 2 && num_kb >= 16) {
-      int splits = std::min<int64_t>(cap / tiles, num_kb / 8);
+    if (tiles < cap / 2 && num_kb >= 32) {
+      // chunks of at least 16 slabs: the fix-up's latency grows with the number of chunks
+      int splits = std::min<int64_t>(cap / tiles, num_kb / 16);
       splits = std::max(1, std::min(splits, 64));
       if (splits > 1) {
         const int kps = (num_kb + splits - 1) / splits;

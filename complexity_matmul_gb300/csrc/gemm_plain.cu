@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc32[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc32[j] = 0.f;
+#pragma unroll 2
             for (int sp = 0; sp < args.splits; ++sp) {
               const float4* src =
                   reinterpret_cast<const float4*>(qbase + (static_cast<int64_t>(sp) * kBM + rl) * BN + c * 32);

@@ -132,19 +132,23 @@ __device__ __forceinline__ void store_block(const SkinnyArgs& a, uint32_t taddr,
 }
 
 // Sum of the block's partials (quarter q, this thread's n) in K order -> C.
-// Runs of 16 m values: every partial load of a run is issued before its sums.
+// Runs of 8 m values; the contributor loop is unrolled so that the loads of
+// several partials are in flight before their (in-order) sums.
 template <int MP, bool BF16, int ACT>
 __device__ __forceinline__ void fixup_block(const SkinnyArgs& a, int blk, int q, int lane, int c_lo, int c_hi, int n,
                                             float bias_n, int grid) {
-  constexpr int W = 16;
+  constexpr int W = 8;
   if (n >= a.N) return;
+  // the block is the first of every contributor's range except possibly c_lo's
+  const int slot_lo = range_begin(c_lo, a.total, grid) == int64_t(blk) * a.num_kb ? 0 : 1;
 #pragma unroll 1
   for (int m0 = 0; m0 < a.M; m0 += W) {
     float v[W];
 #pragma unroll
     for (int i = 0; i < W; ++i) v[i] = 0.f;
+#pragma unroll 4
     for (int c = c_lo; c <= c_hi; ++c) {
-      const int slot = (blk == range_begin(c, a.total, grid) / a.num_kb) ? 0 : 1;
+      const int slot = c == c_lo ? slot_lo : 0;
       const float* p = a.partial + ((static_cast<int64_t>(c) * 2 + slot) * MP + m0) * kRowsB + q * 32 + lane;
       float x[W];
 #pragma unroll

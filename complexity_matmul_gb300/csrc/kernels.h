@@ -94,7 +94,7 @@ struct SkinnyLaunch {
 };
 cudaError_t launch_skinny(const SkinnyLaunch& L, cudaStream_t stream);
 constexpr int kSkinnyMaxM = 256;
-constexpr int kSkinnyMinKPerCta = 512;     // grid = min(SMs, ceil(K iterations / 512 deep))
+constexpr int kSkinnyMinKPerCta = 1024;    // grid = min(SMs, ceil(K iterations / 1024 deep))
 
 // GEMV-shaped products (M <= 4) on the CUDA cores (gemv.cu).
 struct GemvArgs {
