@@ -166,13 +166,16 @@ int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K) {
   if (h->plain_kernel == 1) return 1;
   if (h->plain_kernel == 2) return grid_cap(h) < 2 ? 1 : 2;
   // measured choices: one or two rows stream B best on the CUDA cores (at four
-  // the FMA work makes the tiled split-K kernel faster); up to 128 rows with
-  // few 256-column tiles and a long K (where the tiled kernel would need a deep
-  // K split), the stream-K skinny kernel
+  // the FMA work makes the tiled split-K kernel faster); CTA pairs once their
+  // 256 x 256 tiles fill a quarter of the pairs' slots; otherwise the single-CTA
+  // tiles, whose split-K spreads a few tiles over the machine.  (The stream-K
+  // skinny kernel measured at best level with split-K since the latter's deep
+  // splits are summed by a separate kernel; it stays available as an option.)
+  (void)K;
   if (M <= 2) return 4;
-  if (skinny_ok && M <= 128 && N >= 1024 && N <= 8192 && K >= 2 * N) return 3;
   if (grid_cap(h) < 2) return 1;
-  return (M > 128 && N > 128) ? 2 : 1;
+  const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  return (M > 128 && N > 128 && pair_tiles >= grid_cap(h) / 4) ? 2 : 1;
 }
 
 int run_gemv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
@@ -303,7 +306,11 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
         a.kb_per_split = kps;
         a.partial = static_cast<float*>(h->ws);
         a.counters = reinterpret_cast<int*>(static_cast<char*>(h->ws) + off);
-        if (cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+        // with many chunks the last arriver's serial sum is latency-bound: a
+        // separate, fully parallel reduction is faster, and needs no counters
+        a.reduce_separately = splits >= kSeparateReduceSplits ? 1 : 0;
+        if (!a.reduce_separately && cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess)
+          return LCGEMM_ERR_CUDA;
       }
     }
   }
@@ -331,7 +338,9 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     return launch_plain_pair(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
   }
   L.grid = static_cast<int>(std::min<int64_t>(tiles * a.splits, grid_cap(h)));
-  return launch_plain(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+  if (launch_plain(L, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  if (a.reduce_separately && launch_splitk_reduce(L, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  return LCGEMM_OK;
 }
 
 }  // namespace lcg

@@ -256,6 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (args.reduce_separately) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+          continue;
+        }
         // The last chunk to arrive (per tile and lane quarter: no cross-warp
         // barrier, no waiting) sums all chunks' partials in chunk order.
         __threadfence();
@@ -316,6 +321,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Split-K reduction: one thread per 8 consecutive columns of one valid row of
+// a tile; the partials of its chunks are summed in chunk order (four chunks'
+// loads in flight at a time), then epilogue, one rounding, store.
+template <int BN, bool BF16>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const PlainArgs a) {
+  const int64_t vec_per_row = BN / 8;
+  const int64_t total = int64_t(a.num_tiles) * kBM * vec_per_row;
+  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
+    const int tile = static_cast<int>(v / (kBM * vec_per_row));
+    const int64_t rem = v - int64_t(tile) * kBM * vec_per_row;
+    const int r = static_cast<int>(rem / vec_per_row);
+    const int c8 = static_cast<int>(rem - int64_t(r) * vec_per_row) * 8;
+    int mb, nb;
+    tile_coords(tile, a, mb, nb);
+    const int64_t row = int64_t(mb) * kBM + r;
+    const int64_t col = int64_t(nb) * BN + c8;
+    if (row >= a.M || col >= a.N) continue;
+    const float* p = a.partial + (int64_t(tile) * a.splits * kBM + r) * BN + c8;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float4* q = reinterpret_cast<const float4*>(p + int64_t(sp) * kBM * BN);
+      const float4 x = __ldcg(q), y = __ldcg(q + 1);
+      s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
+      s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
+    }
+    const int n = static_cast<int>(a.N - col < 8 ? a.N - col : 8);
+    uint16_t* C = static_cast<uint16_t*>(a.C) + row * a.ldc + col;
+    if (a.ep.on) store_run<BF16, 8>(C, row, col, n, s, a.ep);
+    else cast_store<BF16, 8>(C, n, s);
+  }
+}
+
 template <int BN, int STAGES, bool BF16, bool EPI>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
@@ -330,7 +368,24 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int BN, bool BF16>
+cudaError_t launch_reduce_impl(const PlainLaunch& L, int num_sms, cudaStream_t stream) {
+  const int64_t total = int64_t(L.args.num_tiles) * kBM * (BN / 8);
+  int64_t blocks = (total + 255) / 256;
+  blocks = blocks < int64_t(num_sms) * 8 ? blocks : int64_t(num_sms) * 8;
+  splitk_reduce_kernel<BN, BF16><<<static_cast<int>(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(L.args);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_splitk_reduce(const PlainLaunch& L, int num_sms, cudaStream_t stream) {
+  if (L.bn == 256) return L.bf16 ? launch_reduce_impl<256, true>(L, num_sms, stream)
+                                 : launch_reduce_impl<256, false>(L, num_sms, stream);
+  if (L.bn == 128) return L.bf16 ? launch_reduce_impl<128, true>(L, num_sms, stream)
+                                 : launch_reduce_impl<128, false>(L, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream) {
   // the kernel without an epilogue keeps the lean store path

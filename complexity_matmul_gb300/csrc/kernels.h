@@ -45,6 +45,9 @@ struct PlainArgs {
   int tail_first;
   int num_items;
   Epilogue ep;
+  // split-K with many chunks: the chunks only publish their partials and a
+  // separate reduction kernel sums them (every output element in parallel)
+  int reduce_separately;
 };
 
 struct PlainLaunch {
@@ -60,6 +63,10 @@ constexpr int kPlainBM = 128;
 constexpr int kPlainBK = 64;
 
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream);
+// Split-K with at least this many chunks sums them in a separate kernel.
+constexpr int kSeparateReduceSplits = 4;
+// Sum of the split-K partials of launch L in chunk order, epilogue, one rounding (after launch_plain).
+cudaError_t launch_splitk_reduce(const PlainLaunch& L, int num_sms, cudaStream_t stream);
 // CTA-pair variant: 256 x 256 tiles per cluster of two; tensor maps use 128-row boxes for A and B.
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 

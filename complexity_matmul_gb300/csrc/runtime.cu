@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "kernels.h"
 #include "lcgemm.h"
 #include "runtime.h"
 
@@ -84,7 +85,9 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
   const double mnk2 = 2.0 * m * n * k;
   if (algo == LCGEMM_PLAIN) {
     const double bytes = 2.0 * (m * k + k * n + m * n);
-    const bool pair = sms >= 2 && (h->plain_kernel == 2 || (h->plain_kernel == 0 && M > 128 && N > 128));
+    const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
+    const bool pair = sms >= 2 && (h->plain_kernel == 2 ||
+                                   (h->plain_kernel == 0 && M > 128 && N > 128 && pair_tiles >= sms / 4));
     if (pair) {
       // the partial last wave runs as K halves when it fits twice over
       const int64_t tiles = cdiv(M, 256) * cdiv(N, 256);
@@ -95,8 +98,16 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
         eff = static_cast<double>(tiles) / ((static_cast<double>(full) + 0.5) * units);
       return std::max(mnk2 / (kEtaPlainPair * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
     }
+    // single-CTA tiles with the launcher's split-K: tiles x chunks work items, FP32
+    // partials written and read back, deep splits summed by a separate kernel
     const int64_t bn = N <= 128 ? 128 : 256;
-    return kernel_time(mnk2, bytes, cdiv(M, 128) * cdiv(N, bn), sms, kEtaPlainSingle, P, BW);
+    const int64_t tiles = cdiv(M, 128) * cdiv(N, bn), num_kb = cdiv(K, 64);
+    int64_t splits = 1;
+    if (tiles < sms / 2 && num_kb >= 32) splits = std::max<int64_t>(1, std::min<int64_t>(sms / tiles, num_kb / 16));
+    const double part_bytes = splits > 1 ? 2.0 * 4.0 * static_cast<double>(tiles * splits) * 128.0 * bn : 0.0;
+    double t = kernel_time(mnk2, bytes + part_bytes, tiles * splits, sms, kEtaPlainSingle, P, BW);
+    if (splits >= kSeparateReduceSplits) t += kernel_time(0, part_bytes / 2 + 2.0 * m * n, 0, 1, 1.0, P, BW);
+    return t;
   }
   if (!algo_supported(algo, M, N, K)) return INFINITY;
   // non-divisible shapes run on zero-padded copies: the copy (read the operands,
