@@ -98,12 +98,12 @@ enum {
   LCGEMM_OPT_HBM_GBPS = 6,         /* cost model: HBM bandwidth, GB/s                                 */
   LCGEMM_OPT_DEBUG_DROP_SIGNAL = 7, /* test hook: a split Group's partner never signals, so the
                                       owner's bounded wait runs out (no fault, no hang)               */
-  LCGEMM_OPT_PLAIN_KERNEL = 8,      /* plain GEMM kernel: 0 choose (default: GEMV for M <= 2; the
-                                      skinny kernel for M <= 128 when N <= 8192 and K >= 2N; CTA
-                                      pairs when M, N > 128; else single-CTA), 1 single-CTA 128x256
-                                      tiles, 2 CTA-pair (cta_group::2) 256x256 tiles, 3 the stream-K
-                                      skinny kernel (M <= 256), 4 the CUDA-core GEMV (M <= 4); for
-                                      3 and 4 larger M choose                                          */
+  LCGEMM_OPT_PLAIN_KERNEL = 8,      /* plain GEMM kernel: 0 choose (default: the GEMV for M <= 2; CTA
+                                      pairs when M, N > 128 and their 256x256 tiles fill a quarter of
+                                      the pairs; else single-CTA tiles with split-K), 1 single-CTA
+                                      128x256 tiles, 2 CTA-pair (cta_group::2) 256x256 tiles, 3 the
+                                      stream-K skinny kernel (M <= 256), 4 the CUDA-core GEMV
+                                      (M <= 4); for 3 and 4 larger M choose                            */
   LCGEMM_OPT_LCMA_KERNEL = 9        /* fused one-level Strassen kernel: 0 choose (default), 1
                                       single-CTA 128x128 Groups, 2 CTA-pair 256x128 Groups           */
 };

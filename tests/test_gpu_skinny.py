@@ -95,8 +95,8 @@ def test_in_place_residual(h):
 
 
 def test_default_choice_and_fallback():
-    """Without an option, 64 x 512 x 1024 (M <= 128, N <= 8192, K >= 2N) runs the skinny kernel; the
-    option on M > 256 falls back to the tiled kernels."""
+    """Without an option 64 x 512 x 1024 runs the default (tiled) kernel; the skinny option on M > 256
+    falls back to the tiled kernels."""
     hd = lcg.Handle(0)
     try:
         A, B = synthetic.operands(64, 512, 1024, "int3", 80, "bf16", "cuda")
