@@ -85,7 +85,7 @@ def _kernel_source_hash(name: str) -> str:
     path = os.path.join(ROOT, "complexity_matmul_gb300", "csrc", name)
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "complexity_matmul_gb300", "csrc")
-    for p in sorted([path, os.path.join(csrc, "ptx.cuh"), os.path.join(csrc, "epilogue.cuh")]):
+    for p in sorted([path] + [os.path.join(csrc, hdr) for hdr in ("ptx.cuh", "epilogue.cuh", "plain_common.cuh")]):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

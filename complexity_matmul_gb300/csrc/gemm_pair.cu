@@ -19,8 +19,8 @@
 //   empty[s]  one per CTA; the leader's MMA commit arrives on both
 //   tfull[b]  one per CTA; the leader's MMA commit arrives on both
 //   tempty[b] leader's barrier; all 8 epilogue warps of the pair arrive
-#include "epilogue.cuh"
 #include "kernels.h"
+#include "plain_common.cuh"
 #include "ptx.cuh"
 
 namespace lcg {
@@ -39,16 +39,6 @@ constexpr int kTxBytes = 2 * kStageBytes;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
 
-__device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& mb, int& nb) {
-  const int group_tiles = a.group_m * a.tiles_n;
-  const int g = tile / group_tiles;
-  const int first_m = g * a.group_m;
-  const int rows = min(a.tiles_m - first_m, a.group_m);
-  const int local = tile - g * group_tiles;
-  mb = first_m + local % rows;
-  nb = local / rows;
-}
-
 // Work item -> tile and K-slab range.  Items below tail_first are whole tiles;
 // the rest are the two K halves of the tiles of the partial last wave.
 __device__ __forceinline__ void pair_item(int w, const PlainArgs& a, int num_kb, int& tile, int& kb0, int& kb1,
@@ -66,32 +56,6 @@ __device__ __forceinline__ void pair_item(int w, const PlainArgs& a, int num_kb,
     kb0 = half ? mid : 0;
     kb1 = half ? num_kb : mid;
   }
-}
-
-__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-// Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
-template <bool BF16, bool EPI>
-__device__ __forceinline__ void store_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
-                                            const PlainArgs& args, const EpiLoads<32>* pre = nullptr) {
-  if (row >= args.M || col >= args.N) return;
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if constexpr (EPI) store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
-  else cast_store<BF16, 32>(crow + col, min(32, args.N - col), v);
-}
-
-// Issues the bias / residual loads of the 32-column chunk at (row, col), if it lies in C.
-__device__ __forceinline__ void load_chunk(int row, int col, const PlainArgs& args, EpiLoads<32>& pre) {
-  if (row < args.M && col < args.N)
-    epilogue_load<32>(args.ep, row, col, min(32, args.N - col), pre);
-  else
-    pre.vb = pre.vr = false;
 }
 
 template <bool BF16, bool EPI>

@@ -12,8 +12,8 @@
 // Prior art for the tiling, the multi-stage prefetch and the block swizzle:
 // CUDA-L2 summary (gist.science 2512.02551), "discovered techniques" list
 // (double-buffering, multi-step prefetch, block swizzling for L2 hit rate).
-#include "epilogue.cuh"
 #include "kernels.h"
+#include "plain_common.cuh"
 #include "ptx.cuh"
 
 namespace lcg {
@@ -35,42 +35,6 @@ struct Cfg {
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
-
-__device__ __forceinline__ void tile_coords(int tile, const PlainArgs& a, int& mb, int& nb) {
-  const int group_tiles = a.group_m * a.tiles_n;
-  const int g = tile / group_tiles;
-  const int first_m = g * a.group_m;
-  const int rows = min(a.tiles_m - first_m, a.group_m);
-  const int local = tile - g * group_tiles;
-  mb = first_m + local % rows;
-  nb = local / rows;
-}
-
-// Epilogue, cast and store of 32 FP32 values of one C row (columns col .. col+31, clipped to C).
-template <bool BF16, bool EPI>
-__device__ __forceinline__ void store_row_chunk(uint16_t* crow, int row, int col, const uint32_t (&r)[32],
-                                                const PlainArgs& args, const EpiLoads<32>* pre = nullptr) {
-  if (row >= args.M || col >= args.N) return;
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if constexpr (EPI) store_run<BF16, 32>(crow + col, row, col, min(32, args.N - col), v, args.ep, pre);
-  else cast_store<BF16, 32>(crow + col, min(32, args.N - col), v);
-}
-
-// Issues the bias / residual loads of the 32-column chunk at (row, col), if it lies in C.
-__device__ __forceinline__ void load_chunk(int row, int col, const PlainArgs& args, EpiLoads<32>& pre) {
-  if (row < args.M && col < args.N)
-    epilogue_load<32>(args.ep, row, col, min(32, args.N - col), pre);
-  else
-    pre.vb = pre.vr = false;
-}
-
-__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
 template <int BN, int STAGES, bool BF16, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -225,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const EpiLoads<32> cur = pre;
             if (c + 1 < BN / 32) load_chunk(row, nb * BN + (c + 1) * 32, args, pre);
             tmem_wait_ld();
-            store_row_chunk<BF16, true>(crow, row, nb * BN + c * 32, r, args, &cur);
+            store_chunk<BF16, true>(crow, row, nb * BN + c * 32, r, args, &cur);
           }
         } else {
 #pragma unroll 1
@@ -233,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             tmem_ld_32x32b_x32(tbase + c * 32, r);
             tmem_wait_ld();
-            store_row_chunk<BF16, false>(crow, row, nb * BN + c * 32, r, args);
+            store_chunk<BF16, false>(crow, row, nb * BN + c * 32, r, args);
           }
         }
         tc_fence_before();
@@ -303,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc32[j]);
-            store_row_chunk<BF16, EPI>(Cp + static_cast<int64_t>(urow) * args.ldc, urow, nb * BN + c * 32, r, args,
+            store_chunk<BF16, EPI>(Cp + static_cast<int64_t>(urow) * args.ldc, urow, nb * BN + c * 32, r, args,
                                        &pre);
           }
         }
