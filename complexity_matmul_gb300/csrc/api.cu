@@ -226,7 +226,9 @@ int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, in
   a.partial = static_cast<float*>(h->ws);
   // arrival counters: zeroed once when (re)allocated; the epoch tag retires old arrivals
   const size_t nctr = static_cast<size_t>(a.nblk) * 4;
+  const bool in_graph = capturing(st);
   if (nctr > h->skinny_ctr_n) {
+    if (in_graph) return LCGEMM_ERR_CAPTURE;
     if (h->skinny_ctr) {
       cudaStreamSynchronize(st);
       cudaFree(h->skinny_ctr);
@@ -243,13 +245,20 @@ int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, in
     h->skinny_ctr_n = nctr;
     h->epoch = 0;
   }
-  if (++h->epoch == 0) {   // 2^32 launches: start the tags over from zeroed counters
-    if (cudaMemsetAsync(h->skinny_ctr, 0, h->skinny_ctr_n * sizeof(unsigned long long), st) != cudaSuccess)
+  if (in_graph) {
+    // a graph replays this launch with the same epoch: reset the block counters in the graph too
+    if (cudaMemsetAsync(h->skinny_ctr, 0, nctr * sizeof(unsigned long long), st) != cudaSuccess)
       return LCGEMM_ERR_CUDA;
-    h->epoch = 1;
+    a.epoch = 1;
+  } else {
+    if (++h->epoch == 0) {   // 2^32 launches: start the tags over from zeroed counters
+      if (cudaMemsetAsync(h->skinny_ctr, 0, h->skinny_ctr_n * sizeof(unsigned long long), st) != cudaSuccess)
+        return LCGEMM_ERR_CUDA;
+      h->epoch = 1;
+    }
+    a.epoch = h->epoch;
   }
   a.counters = h->skinny_ctr;
-  a.epoch = h->epoch;
   a.err = h->err_dev;
   a.timeout_ns = h->timeout_ns;
   a.ep = ep;
@@ -474,6 +483,7 @@ int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, 
   DeviceGuard g(h->device);
   if (!g.ok) return LCGEMM_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (capturing(st)) return LCGEMM_ERR_CAPTURE;   // copy streams and host buffers: not capturable
   // device staging: pitches rounded up to 8 elements (16 bytes), 256-byte aligned sub-buffers
   const int64_t kp = std::max<int64_t>(8, (K + 7) / 8 * 8);
   const int64_t np = (N + 7) / 8 * 8;
@@ -643,6 +653,7 @@ const char* lcgemm_strerror(int code) {
     case LCGEMM_ERR_TIMEOUT: return "a bounded device-side wait gave up in an earlier launch";
     case LCGEMM_ERR_NOMEM: return "workspace allocation failed";
     case LCGEMM_ERR_TOO_LARGE: return "problem too large for the fixed scratch of lcgemm_strassen1_noalloc";
+    case LCGEMM_ERR_CAPTURE: return "stream capture: the call would grow a handle buffer, or cannot be captured";
     default: return "unknown status code";
   }
 }

@@ -16,9 +16,19 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
+bool capturing(cudaStream_t st) {
+  cudaStreamCaptureStatus s = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &s) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return s != cudaStreamCaptureStatusNone;
+}
+
 // Grow the handle's workspace to at least `bytes` (stream-ordered with `st`).
 int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st) {
   if (bytes <= h->ws_bytes) return LCGEMM_OK;
+  if (capturing(st)) return LCGEMM_ERR_CAPTURE;
   if (h->ws) {
     cudaStreamSynchronize(st);
     cudaFree(h->ws);
@@ -181,6 +191,7 @@ int run_strassen(lcgemm_ctx* h, int levels, bool fused, int64_t M, int64_t N, in
     const int64_t a_bytes = pad_a ? round_up(Mp * Kp * 2, 256) : 0, b_bytes = pad_b ? round_up(Np * Kp * 2, 256) : 0;
     const size_t need = static_cast<size_t>(a_bytes + b_bytes);
     if (need > h->pad_bytes) {
+      if (capturing(st)) return LCGEMM_ERR_CAPTURE;
       if (h->pad) {
         cudaStreamSynchronize(st);
         cudaFree(h->pad);

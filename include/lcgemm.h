@@ -43,6 +43,14 @@
  * Threading: a handle may be used by one host thread at a time, and runs
  * through one handle must not overlap on different streams (they share the
  * handle's workspace).
+ *
+ * CUDA graphs: lcgemm_run and lcgemm_run_epilogue may be captured into a graph
+ * (stream capture) and the graph replayed, provided each captured shape has
+ * run once on the handle outside the capture, so that the workspace and the
+ * other handle-owned buffers already have their size (a call that would grow
+ * one returns LCGEMM_ERR_CAPTURE and captures nothing).  Device pointers and
+ * sizes are fixed in the graph; replays read the buffers' current contents.
+ * lcgemm_run_host cannot be captured.
  */
 #ifndef LCGEMM_H
 #define LCGEMM_H
@@ -85,7 +93,9 @@ enum {
   LCGEMM_ERR_CUDA = -5,         /* a CUDA runtime/driver call or launch failed            */
   LCGEMM_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up (earlier launch)    */
   LCGEMM_ERR_NOMEM = -7,        /* workspace or staging allocation failed                 */
-  LCGEMM_ERR_TOO_LARGE = -8     /* problem exceeds lcgemm_strassen1_noalloc's fixed scratch */
+  LCGEMM_ERR_TOO_LARGE = -8,    /* problem exceeds lcgemm_strassen1_noalloc's fixed scratch */
+  LCGEMM_ERR_CAPTURE = -9       /* the stream is capturing a CUDA graph and the call would have
+                                   to grow a handle buffer (or it is lcgemm_run_host)       */
 };
 
 /* options for lcgemm_set_option */
