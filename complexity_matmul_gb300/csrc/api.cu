@@ -415,8 +415,7 @@ int lcgemm_destroy(lcgemm_t h) {
   if (h->stage) cudaFree(h->stage);
   if (h->skinny_ctr) cudaFree(h->skinny_ctr);
   if (h->pad) cudaFree(h->pad);
-  for (int i = 0; i < lcgemm_ctx::kHostEvents; ++i)
-    if (h->ev[i]) cudaEventDestroy(h->ev[i]);
+  for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
   if (h->copy_in) cudaStreamDestroy(h->copy_in);
   if (h->copy_out) cudaStreamDestroy(h->copy_out);
   if (h->err_host) cudaFreeHost(h->err_host);
@@ -465,14 +464,15 @@ int lcgemm_run_epilogue(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void*
   return rc;
 }
 
-// Host buffers: B is copied first; A is copied in row chunks on a copy stream,
-// each chunk's GEMM runs on the caller's stream as soon as its rows arrive, and
-// each chunk of C goes back on a second copy stream -- host->device copies,
-// tensor-core work and device->host copies overlap.  Plain GEMMs (explicit or
-// chosen by the cost model) are chunked; a chunk may sum the K range in a
-// different FP32 order than the whole GEMM would (tail splits depend on the
-// tile count), so results agree to FP32 rounding, not bit for bit.  Strassen
-// runs unchunked.
+// Host buffers: plain GEMMs (explicit or chosen by the cost model) run as a grid
+// of C blocks.  A row chunks and B column chunks go to the device alternately on
+// a copy stream (A0, B0, A1, B1, ...); each block's GEMM runs on the caller's
+// stream as soon as its two chunks have arrived, and each block of C goes back on
+// a second copy stream -- host->device copies, tensor-core work and
+// device->host copies overlap, and the first GEMM waits for two chunks instead
+// of all of B.  A block may sum the K range in a different FP32 order than the
+// whole GEMM would (split choices depend on the tile count), so results agree to
+// FP32 rounding, not bit for bit.  Strassen runs unchunked.
 int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int dtype, int algo, void* cuda_stream) {
   if (!h || h->device == LCGEMM_PLANNING_DEVICE) return LCGEMM_ERR_ARG;
@@ -516,9 +516,15 @@ int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, 
                : LCGEMM_ERR_CUDA;
   }
   const int chosen = algo == LCGEMM_AUTO ? select_algo(h, M, N, K, dtype) : algo;
-  int chunks = 1;
-  if (chosen == LCGEMM_PLAIN) chunks = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, M / 2048)));
-  if (chunks == 1) {
+  // Plain GEMMs run as a grid of nr x nc blocks of C (2048-row/column chunks, at
+  // most 8 x 8), so that the first block can start as soon as one chunk of A and
+  // one of B have arrived, instead of after all of B.
+  int nr = 1, nc = 1;
+  if (chosen == LCGEMM_PLAIN) {
+    nr = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, M / 2048)));
+    nc = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, N / 2048)));
+  }
+  if (nr * nc == 1) {
     if (cudaMemcpy2DAsync(dA, kp * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpy2DAsync(dB, kp * 2, B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, st) != cudaSuccess)
       return LCGEMM_ERR_CUDA;
@@ -532,38 +538,71 @@ int lcgemm_run_host(lcgemm_t h, int64_t M, int64_t N, int64_t K, const void* A, 
     if (cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking) != cudaSuccess)
       return LCGEMM_ERR_CUDA;
-    for (int i = 0; i < lcgemm_ctx::kHostEvents; ++i)
-      if (cudaEventCreateWithFlags(&h->ev[i], cudaEventDisableTiming) != cudaSuccess) return LCGEMM_ERR_CUDA;
   }
-  cudaEvent_t* ev = h->ev;   // [0] start, [1] B in, [2..2+c) A chunk in, [2+c..2+2c) C chunk done, [2+2c] out
-  const int64_t rows = ((M + chunks - 1) / chunks + 255) / 256 * 256;   // chunk rows, a multiple of 256
+  // events: [0] start, [1, 1 + nr) A chunk i in, [1 + nr, 1 + nr + nc) B chunk j in,
+  // then one per C block done, and the last: every block copied out
+  const size_t need_ev = 2 + static_cast<size_t>(nr + nc + nr * nc);
+  while (h->ev.size() < need_ev) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    h->ev.push_back(e);
+  }
+  cudaEvent_t* ev = h->ev.data();
+  cudaEvent_t* ev_a = ev + 1;
+  cudaEvent_t* ev_b = ev + 1 + nr;
+  cudaEvent_t* ev_c = ev + 1 + nr + nc;
+  cudaEvent_t ev_out = ev[need_ev - 1];
+  const int64_t rows = ((M + nr - 1) / nr + 255) / 256 * 256;   // chunk extents, multiples of 256
+  const int64_t cols = ((N + nc - 1) / nc + 255) / 256 * 256;
+  nr = static_cast<int>((M + rows - 1) / rows);
+  nc = static_cast<int>((N + cols - 1) / cols);
   bool ok = cudaEventRecord(ev[0], st) == cudaSuccess && cudaStreamWaitEvent(h->copy_in, ev[0], 0) == cudaSuccess &&
             cudaStreamWaitEvent(h->copy_out, ev[0], 0) == cudaSuccess;
-  ok = ok && cudaMemcpy2DAsync(dB, kp * 2, B, ldb * 2, K * 2, N, cudaMemcpyHostToDevice, h->copy_in) == cudaSuccess &&
-       cudaEventRecord(ev[1], h->copy_in) == cudaSuccess;
-  int n = 0;
-  for (int64_t r0 = 0; ok && r0 < M; r0 += rows, ++n) {
-    const int64_t mr = std::min(rows, M - r0);
-    ok = cudaMemcpy2DAsync(dA + r0 * kp * 2, kp * 2, static_cast<const char*>(A) + r0 * lda * 2, lda * 2, K * 2, mr,
-                           cudaMemcpyHostToDevice, h->copy_in) == cudaSuccess &&
-         cudaEventRecord(ev[2 + n], h->copy_in) == cudaSuccess;
-  }
-  ok = ok && cudaStreamWaitEvent(st, ev[1], 0) == cudaSuccess;
-  n = 0;
-  for (int64_t r0 = 0; ok && r0 < M; r0 += rows, ++n) {
-    const int64_t mr = std::min(rows, M - r0);
-    ok = cudaStreamWaitEvent(st, ev[2 + n], 0) == cudaSuccess;
-    if (ok) {
-      rc = lcgemm_run(h, mr, N, K, dA + r0 * kp * 2, kp, dB, kp, dC + r0 * np * 2, np, dtype, LCGEMM_PLAIN, cuda_stream);
-      if (rc) return rc;
+  const auto copy_a = [&](int i) {
+    const int64_t r0 = i * rows, mr = std::min(rows, M - r0);
+    return cudaMemcpy2DAsync(dA + r0 * kp * 2, kp * 2, static_cast<const char*>(A) + r0 * lda * 2, lda * 2, K * 2,
+                             mr, cudaMemcpyHostToDevice, h->copy_in) == cudaSuccess &&
+           cudaEventRecord(ev_a[i], h->copy_in) == cudaSuccess;
+  };
+  const auto copy_b = [&](int j) {
+    const int64_t c0 = j * cols, nn = std::min(cols, N - c0);
+    return cudaMemcpy2DAsync(dB + c0 * kp * 2, kp * 2, static_cast<const char*>(B) + c0 * ldb * 2, ldb * 2, K * 2,
+                             nn, cudaMemcpyHostToDevice, h->copy_in) == cudaSuccess &&
+           cudaEventRecord(ev_b[j], h->copy_in) == cudaSuccess;
+  };
+  const auto block = [&](int i, int j) -> int {
+    const int64_t r0 = i * rows, mr = std::min(rows, M - r0), c0 = j * cols, nn = std::min(cols, N - c0);
+    if (cudaStreamWaitEvent(st, ev_a[i], 0) != cudaSuccess || cudaStreamWaitEvent(st, ev_b[j], 0) != cudaSuccess)
+      return LCGEMM_ERR_CUDA;
+    const int r = lcgemm_run(h, mr, nn, K, dA + r0 * kp * 2, kp, dB + c0 * kp * 2, kp, dC + (r0 * np + c0) * 2, np,
+                             dtype, LCGEMM_PLAIN, cuda_stream);
+    if (r) return r;
+    cudaEvent_t e = ev_c[i * nc + j];
+    const bool out = cudaEventRecord(e, st) == cudaSuccess && cudaStreamWaitEvent(h->copy_out, e, 0) == cudaSuccess &&
+                     cudaMemcpy2DAsync(static_cast<char*>(C) + (r0 * ldc + c0) * 2, ldc * 2,
+                                       dC + (r0 * np + c0) * 2, np * 2, nn * 2, mr, cudaMemcpyDeviceToHost,
+                                       h->copy_out) == cudaSuccess;
+    return out ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+  };
+  // growing square: A chunk k, then the blocks it completes with B chunks < k;
+  // B chunk k, then the blocks it completes with A chunks <= k
+  for (int k = 0; ok && k < std::max(nr, nc); ++k) {
+    if (k < nr) {
+      ok = copy_a(k);
+      for (int j = 0; ok && j < std::min(k, nc); ++j) {
+        rc = block(k, j);
+        if (rc) return rc;
+      }
     }
-    ok = ok && cudaEventRecord(ev[2 + chunks + n], st) == cudaSuccess &&
-         cudaStreamWaitEvent(h->copy_out, ev[2 + chunks + n], 0) == cudaSuccess &&
-         cudaMemcpy2DAsync(static_cast<char*>(C) + r0 * ldc * 2, ldc * 2, dC + r0 * np * 2, np * 2, N * 2, mr,
-                           cudaMemcpyDeviceToHost, h->copy_out) == cudaSuccess;
+    if (ok && k < nc) {
+      ok = copy_b(k);
+      for (int i = 0; ok && i < std::min(k + 1, nr); ++i) {
+        rc = block(i, k);
+        if (rc) return rc;
+      }
+    }
   }
-  ok = ok && cudaEventRecord(ev[2 + 2 * chunks], h->copy_out) == cudaSuccess &&
-       cudaStreamWaitEvent(st, ev[2 + 2 * chunks], 0) == cudaSuccess;
+  ok = ok && cudaEventRecord(ev_out, h->copy_out) == cudaSuccess && cudaStreamWaitEvent(st, ev_out, 0) == cudaSuccess;
   if (!ok) return LCGEMM_ERR_CUDA;
   h->last_algo = LCGEMM_PLAIN;
   return LCGEMM_OK;

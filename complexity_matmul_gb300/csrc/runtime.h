@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,8 +34,7 @@ struct lcgemm_ctx {
   size_t stage_bytes = 0;
   // lcgemm_run_host pipeline: copy streams (host->device, device->host) and events
   cudaStream_t copy_in = nullptr, copy_out = nullptr;
-  static constexpr int kHostEvents = 24;
-  cudaEvent_t ev[kHostEvents] = {};
+  std::vector<cudaEvent_t> ev;
 };
 
 namespace lcg {

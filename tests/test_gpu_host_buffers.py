@@ -28,11 +28,13 @@ def _run_host(h, A, B, C, algo):
     return rc
 
 
-@pytest.mark.parametrize("M,N,K", [(8192, 2048, 1024), (4096, 1000, 520), (300, 260, 136), (6000, 512, 256)])
+@pytest.mark.parametrize("M,N,K", [(8192, 2048, 1024), (4096, 1000, 520), (300, 260, 136), (6000, 512, 256),
+                                   (4100, 4200, 512), (8192, 8192, 256), (2048, 10000, 128)])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_buffers_match_device_path(h, M, N, K, pinned):
-    """The row-chunked, pipelined host path gives the device path's result: bit for bit on
-    integer inputs, and to FP32 summation order on N(0,1) inputs (at most one BF16 ulp apart)."""
+    """The block-gridded, pipelined host path (ragged edge blocks included) gives the device path's
+    result: bit for bit on integer inputs, and to FP32 summation order on N(0,1) inputs (at most one
+    BF16 ulp apart)."""
     for dist in ("int3", "normal"):
         A, B = synthetic.operands(M, N, K, dist, 31, "bf16", "cuda")
         ref = h.run(A, B, algo="plain").cpu()
