@@ -91,3 +91,26 @@ def test_peak_and_bandwidth_options_move_the_choice(plan):
     with pytest.raises(lcg.LcgemmError):
         h.set_option(lcg.OPT_PEAK_GFLOPS, 0)
     h.close()
+
+
+def test_few_tile_long_k_shapes_use_split_k(plan):
+    """A 128 x 512 output with K = 16384 has two 128 x 256 tiles: the model spreads them over the
+    machine as split-K work items (measured ~25 us on GB300), not two CTAs walking 256 K slabs."""
+    M, N, K = 128, 512, 16384
+    t = plan.estimate(M, N, K, lcg.BF16, "plain")
+    one_cta_per_tile = 2.0 * M * N * K / (2.25e15 / 152)          # two tiles, one SM each
+    assert t < 0.5 * one_cta_per_tile
+    assert t < plan.estimate(M, N, K, lcg.BF16, "strassen2")
+    assert plan.select(M, N, K, lcg.BF16) == lcg.PLAIN
+
+
+def test_pair_tiles_only_when_they_fill_the_pairs(plan):
+    """CTA pairs need their 256 x 256 tiles to fill a quarter of the pairs; below that the estimate
+    is the single-CTA split-K one, which for few tiles is lower than the pair estimate."""
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    shape = (256, 4096, 14336)                     # 16 pair tiles on 76 pairs
+    t_default = h.estimate(*shape, lcg.BF16, "plain")
+    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    t_pair = h.estimate(*shape, lcg.BF16, "plain")
+    h.close()
+    assert t_default < t_pair
