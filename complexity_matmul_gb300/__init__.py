@@ -26,7 +26,7 @@ ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 OK, ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_NOMEM = 0, -1, -2, -3, -4, -5, -6, -7
 ERR_TOO_LARGE, ERR_CAPTURE = -8, -9
 OPT_WAIT_TIMEOUT_US, OPT_GROUP_ORDER, OPT_SPLIT, OPT_MAX_CTAS = 1, 2, 3, 4
-OPT_PEAK_GFLOPS, OPT_HBM_GBPS, OPT_DEBUG_DROP_SIGNAL, OPT_PLAIN_KERNEL, OPT_LCMA_KERNEL = 5, 6, 7, 8, 9
+OPT_PEAK_GFLOPS, OPT_HBM_GBPS, OPT_DEBUG_DROP_SIGNAL, OPT_PLAIN_KERNEL, OPT_LCMA_KERNEL, OPT_PDL = 5, 6, 7, 8, 9, 10
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = 0, 1, 2, 3
 ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_GELU_TANH}
 

@@ -672,6 +672,10 @@ int lcgemm_set_option(lcgemm_t h, int option, int64_t value) {
       if (value < 0 || value > 4) return LCGEMM_ERR_ARG;
       h->plain_kernel = static_cast<int>(value);
       return LCGEMM_OK;
+    case LCGEMM_OPT_PDL:
+      if (value < 0 || value > 1) return LCGEMM_ERR_ARG;
+      h->pdl = static_cast<int>(value);
+      return LCGEMM_OK;
     case LCGEMM_OPT_LCMA_KERNEL:
       if (value < 0 || value > 2) return LCGEMM_ERR_ARG;
       h->lcma_kernel = static_cast<int>(value);

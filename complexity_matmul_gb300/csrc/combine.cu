@@ -91,6 +91,7 @@ __device__ __forceinline__ void combine_vec(const CombineSide& s, int64_t v) {
 
 template <int L, bool BF16>
 __global__ void __launch_bounds__(256) combine_ab_kernel(const __grid_constant__ CombineArgs args) {
+  griddep_launch_dependents();   // the product kernel may be scheduled now; it waits for this grid's writes
   const int64_t na = args.side[0].vecs;
   const int64_t total = na + args.side[1].vecs;
   for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(256) combine_ab_kernel(const __grid_constant__
 // C block (R, C) = sum_p W[(R,C), p] * P_p, FP32 products [R][Mb][ldp] -> C (dtype).
 template <int L, bool BF16>
 __global__ void __launch_bounds__(256) combine_h_kernel(const __grid_constant__ CombineHArgs a) {
+  griddep_wait();   // the products come from the kernel before this one
   constexpr int G = 1 << L;
   constexpr int R = ipow(7, L);
   constexpr WTable<L> wt{};
@@ -197,15 +199,18 @@ cudaError_t launch_pad_copy(const PadArgs& a, int num_sms, cudaStream_t st) {
   return launch_grid_stride(pad_copy_kernel, a, total, num_sms, st);
 }
 
-cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st) {
+cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st, bool pdl) {
   const int64_t total = int64_t(a.mb) * ((a.nb + 3) / 4);
   if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  blocks = blocks < int64_t(num_sms) * 8 ? blocks : int64_t(num_sms) * 8;
+  const int g = static_cast<int>(blocks < 1 ? 1 : blocks);
   if (levels == 1)
-    return bf16 ? launch_grid_stride(combine_h_kernel<1, true>, a, total, num_sms, st)
-                : launch_grid_stride(combine_h_kernel<1, false>, a, total, num_sms, st);
+    return bf16 ? launch_maybe_pdl(combine_h_kernel<1, true>, g, 256, 0, st, pdl, a)
+                : launch_maybe_pdl(combine_h_kernel<1, false>, g, 256, 0, st, pdl, a);
   if (levels == 2)
-    return bf16 ? launch_grid_stride(combine_h_kernel<2, true>, a, total, num_sms, st)
-                : launch_grid_stride(combine_h_kernel<2, false>, a, total, num_sms, st);
+    return bf16 ? launch_maybe_pdl(combine_h_kernel<2, true>, g, 256, 0, st, pdl, a)
+                : launch_maybe_pdl(combine_h_kernel<2, false>, g, 256, 0, st, pdl, a);
   return cudaErrorInvalidValue;
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -162,7 +163,7 @@ struct CombineHArgs {
   Epilogue ep;          // applied in C's coordinates
   int M, N;             // C's extents: blocks of zero-padded operands may reach past them
 };
-cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_combine_h(const CombineHArgs& a, int levels, bool bf16, int num_sms, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- fused LCMA product kernel
 
@@ -201,7 +202,26 @@ struct LcmaLaunch {
   int levels;
   bool bf16;
   int grid;
+  bool pdl;   // launch as a programmatic dependent of the preceding pre-pass kernel
 };
+
+// Launches kern<<<grid, block, smem, st>>>(args...), as a programmatic dependent
+// of the previous kernel in `st` when `pdl` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t st, bool pdl,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 cudaError_t launch_lcma_fused(const LcmaLaunch& L, cudaStream_t st);
 cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st);
 // CTA-pair fused one-level kernel: Groups of 256 x 256 quadrant tiles; A and B maps use 128-row

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      griddep_wait();   // the summed operands come from the pre-pass kernel before this one
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < args.num_groups; t += gridDim.x) {
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      griddep_wait();   // the summed operands come from the pre-pass kernel before this one
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
@@ -391,8 +393,8 @@ cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<L.grid, kThreads, kSmemBytes, st>>>(L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw, L.args);
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw,
+                          L.args);
 }
 
 }  // namespace
@@ -410,9 +412,8 @@ cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  lcma_products_kernel<<<L.grid, kThreads, kSmemBytes, st>>>(L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw, L.args,
-                                                              L.bf16);
-  return cudaGetLastError();
+  return launch_maybe_pdl(lcma_products_kernel, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum,
+                          L.tmB_raw, L.args, L.bf16);
 }
 
 }  // namespace lcg

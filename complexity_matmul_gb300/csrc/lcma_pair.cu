@@ -333,6 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
+      griddep_wait();   // the summed operands come from the pre-pass kernel before this one
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
@@ -487,8 +488,8 @@ cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<L.grid, kThreads, kSmemBytes, st>>>(L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw, L.args);
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw,
+                          L.args);
 }
 
 }  // namespace

@@ -73,6 +73,11 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   CombineArgs ca{};
   ca.side[0] = CombineSide{static_cast<const uint16_t*>(A), lda, wsA, kb, mb * kb, mb, kb, mb * kb / 8};
   ca.side[1] = CombineSide{static_cast<const uint16_t*>(B), ldb, wsB, kb, nb * kb, nb, kb, nb * kb / 8};
+  // the split-Group flags are cleared before the pre-pass, so that the product kernel
+  // directly follows the pre-pass and can be launched as its programmatic dependent
+  int* flags = fused ? reinterpret_cast<int*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes + s_bytes)
+                     : nullptr;
+  if (fused && cudaMemsetAsync(flags, 0, static_cast<size_t>(f_bytes), st) != cudaSuccess) return LCGEMM_ERR_CUDA;
   if (launch_combine_ab(ca, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
 
   // ---- products
@@ -83,6 +88,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   LcmaLaunch ll{};
   ll.levels = L;
   ll.bf16 = bf16;
+  ll.pdl = h->pdl != 0;
   // CTA-pair kernel: summed operands as one 2-D (slots * rows) x kb map; raw
   // blocks as a 2-D map of the whole operand when kb is a multiple of 64.
   const bool raw2d = pair && kb % 64 == 0;
@@ -148,10 +154,9 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
     const bool split = h->split && rem > 0 && 2 * rem <= P;
     a.split_first = split ? full_waves * P : a.num_groups;
     a.num_items = split ? full_waves * P + 2 * rem : a.num_groups;
-    a.flags = split ? reinterpret_cast<int*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes + s_bytes) : nullptr;
+    a.flags = split ? flags : nullptr;
     a.debug_drop = h->debug_drop;
     a.raw2d = raw2d ? 1 : 0;
-    if (split && cudaMemsetAsync(a.flags, 0, sizeof(int) * 2 * rem, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     ll.grid = 2 * std::min(a.num_items, P);
     if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     return LCGEMM_OK;
@@ -165,7 +170,9 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   if (launch_lcma_products(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
   CombineHArgs ch{prod, ldp, static_cast<uint16_t*>(C), ldc, static_cast<int>(mb), static_cast<int>(nb), ep,
                   static_cast<int>(Mc), static_cast<int>(Nc)};
-  if (launch_combine_h(ch, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  // (no programmatic dependency here: measured slower for two levels, whose recombination
+  // blocks would wait on SMs the products still use)
+  if (launch_combine_h(ch, L, bf16, h->num_sms, st, false) != cudaSuccess) return LCGEMM_ERR_CUDA;
   return LCGEMM_OK;
 }
 

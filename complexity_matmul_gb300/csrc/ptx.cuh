@@ -96,6 +96,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+//
+// A kernel launched with programmatic stream serialisation may start while the
+// previous kernel in the stream is still running; griddep_wait() returns once
+// that kernel has completed and its memory operations are visible (at once when
+// there is no such dependency).  griddep_launch_dependents() lets the next
+// kernel be scheduled before this one ends.
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {

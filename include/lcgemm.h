@@ -114,8 +114,11 @@ enum {
                                       128x256 tiles, 2 CTA-pair (cta_group::2) 256x256 tiles, 3 the
                                       stream-K skinny kernel (M <= 256), 4 the CUDA-core GEMV
                                       (M <= 4); for 3 and 4 larger M choose                            */
-  LCGEMM_OPT_LCMA_KERNEL = 9        /* fused one-level Strassen kernel: 0 choose (default), 1
+  LCGEMM_OPT_LCMA_KERNEL = 9,       /* fused one-level Strassen kernel: 0 choose (default), 1
                                       single-CTA 128x128 Groups, 2 CTA-pair 256x128 Groups           */
+  LCGEMM_OPT_PDL = 10               /* 1: launch the Strassen product kernel as a programmatic
+                                      dependent of the pre-pass (its prologue overlaps the pre-pass
+                                      tail; default), 0: plain stream order                           */
 };
 
 /* `device` value of a planning handle (see lcgemm_create). */

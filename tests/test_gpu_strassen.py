@@ -280,3 +280,17 @@ def test_partner_signal_timeout_is_reported_and_recovered():
     assert h2.sync_status() == lcg.OK
     assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
     h2.close()
+
+
+@pytest.mark.parametrize("algo", ["strassen1", "strassen1_unfused", "strassen2"])
+def test_programmatic_dependent_launch_on_off(h, algo):
+    """The product kernel launched as a programmatic dependent of the pre-pass (default) reads the
+    pre-pass's sums only after the pre-pass completes: same bits as plain stream order."""
+    A, B = synthetic.operands(1024, 768, 512, "normal", 14, "bf16", "cuda")
+    out = {}
+    for pdl in (1, 0):
+        h.set_option(lcg.OPT_PDL, pdl)
+        out[pdl] = _run(h, A, B, algo).cpu()
+    h.set_option(lcg.OPT_PDL, 1)
+    assert torch.equal(out[0], out[1])
+    assert_close(out[1].cuda(), oracle_c64(A, B, "bf16"), "bf16", algo)
