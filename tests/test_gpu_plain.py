@@ -220,3 +220,15 @@ def test_argument_errors(h):
     assert run(32, 64, 64, a, 64, b, 64, a + 32 * 64 * 2 - 16, 64, 1, 0) == lcg.ERR_ALIAS
     torch.cuda.synchronize()
     assert h.sync_status() == 0
+
+
+# ---------------------------------------------------------------- extreme aspect ratios
+
+@pytest.mark.parametrize("M,N,K", [(131072, 64, 64), (64, 131072, 64), (64, 64, 1 << 20), (3, 5, 1 << 18)])
+def test_extreme_aspect_ratios_bit_exact(h, M, N, K):
+    """Very tall, very wide and very deep products: thousands of tiles along one dimension, or one
+    tile with a million-deep K (split into the maximum number of chunks)."""
+    A, B = synthetic.operands(M, N, K, "int3", 23, "bf16", "cuda")
+    if K > 1 << 16:
+        A = (A.float() / 8).to(A.dtype)           # |C| <= 9K/8 < 2^24 * 2^-3: exact in FP32
+    assert_bit_exact(_run(h, A, B), oracle_c64(A, B, "bf16"), "bf16")
