@@ -194,10 +194,7 @@ int run_gemv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
   return launch_gemv(a, bf16, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
 }
 
-int skinny_sub(int mp, int64_t K) {
-  if (K <= 64) return 1;
-  return mp <= 64 ? 4 : 2;
-}
+int skinny_sub(int mp, int64_t /*K*/) { return mp <= 64 ? 4 : 2; }
 
 int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {

@@ -389,24 +389,16 @@ cudaError_t launch_impl(const SkinnyLaunch& L, cudaStream_t stream) {
   }
 }
 
-template <int SUB, bool BF16>
+// One stage depth per padded width (the host's skinny_sub): 4 K boxes up to 64
+// rows of A, 2 above (the ring keeps at least two stages).
+template <bool BF16>
 cudaError_t launch_mp(const SkinnyLaunch& L, cudaStream_t stream) {
   switch (L.mp) {
-    case 16: return launch_impl<16, SUB, BF16>(L, stream);
-    case 32: return launch_impl<32, SUB, BF16>(L, stream);
-    case 64: return launch_impl<64, SUB, BF16>(L, stream);
-    case 128: return launch_impl<128, SUB, BF16>(L, stream);
-    case 256: return launch_impl<256, SUB, BF16>(L, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <bool BF16>
-cudaError_t launch_sub(const SkinnyLaunch& L, cudaStream_t stream) {
-  switch (L.sub) {
-    case 1: return launch_mp<1, BF16>(L, stream);
-    case 2: return launch_mp<2, BF16>(L, stream);
-    case 4: return launch_mp<4, BF16>(L, stream);
+    case 16: return L.sub == 4 ? launch_impl<16, 4, BF16>(L, stream) : cudaErrorInvalidValue;
+    case 32: return L.sub == 4 ? launch_impl<32, 4, BF16>(L, stream) : cudaErrorInvalidValue;
+    case 64: return L.sub == 4 ? launch_impl<64, 4, BF16>(L, stream) : cudaErrorInvalidValue;
+    case 128: return L.sub == 2 ? launch_impl<128, 2, BF16>(L, stream) : cudaErrorInvalidValue;
+    case 256: return L.sub == 2 ? launch_impl<256, 2, BF16>(L, stream) : cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -414,7 +406,7 @@ cudaError_t launch_sub(const SkinnyLaunch& L, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_skinny(const SkinnyLaunch& L, cudaStream_t stream) {
-  return L.bf16 ? launch_sub<true>(L, stream) : launch_sub<false>(L, stream);
+  return L.bf16 ? launch_mp<true>(L, stream) : launch_mp<false>(L, stream);
 }
 
 }  // namespace lcg

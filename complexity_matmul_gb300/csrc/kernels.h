@@ -96,7 +96,7 @@ struct SkinnyLaunch {
   CUtensorMap tmA, tmB;            // A: box mp x 64; B: box 128 x 64
   SkinnyArgs args;
   int mp;                          // 16, 32, 64, 128 or 256
-  int sub;                         // 64-deep K boxes per pipeline stage: 1, 2 or 4
+  int sub;                         // 64-deep K boxes per pipeline stage: 4 for mp <= 64, else 2
   bool bf16;
   int grid;
 };
