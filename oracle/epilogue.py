@@ -60,7 +60,8 @@ def activation(x: np.ndarray, act) -> np.ndarray:
     act = ACTS[act] if isinstance(act, str) else int(act)
     if act not in _ACT_FN:
         raise ValueError(f"unknown activation {act}")
-    return _ACT_FN[act](x)
+    with np.errstate(invalid="ignore", over="ignore"):   # IEEE results for inf and NaN inputs, silently
+        return _ACT_FN[act](x)
 
 
 def apply(C64: np.ndarray, bias=None, residual=None, act=ACT_NONE) -> np.ndarray:

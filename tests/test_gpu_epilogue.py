@@ -247,3 +247,21 @@ def test_argument_errors(h):
     assert rc == 0
     torch.cuda.synchronize()
     assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu", "gelu_tanh"])
+def test_special_values_propagate_like_the_oracle(h, act):
+    """Bias entries of +inf, -inf and NaN: every output column takes the oracle's value class (NaN,
+    +inf, -inf or the finite value), e.g. ReLU(NaN) = +0 (x > 0 ? x : 0), GELU(-inf) = NaN."""
+    M, N, K = 64, 256, 64
+    A, B = _int_operands(M, N, K, "bf16", 71)
+    b = _vec(N, "int3", 72, "bf16")
+    b[0], b[1], b[2] = float("inf"), float("-inf"), float("nan")
+    C = _run(h, A, B, bias=b, act=act)
+    D64, pre = oracle_epilogue(A, B, "bf16", b, None, act)
+    got = C.cpu().double().numpy()
+    assert (np.isnan(got) == np.isnan(D64)).all()
+    fin = np.isfinite(D64)
+    assert (np.isinf(got) == np.isinf(D64)).all() and (np.sign(got[~fin & ~np.isnan(D64)]) ==
+                                                       np.sign(D64[~fin & ~np.isnan(D64)])).all()
+    assert_epilogue_close(C[:, 3:], D64[:, 3:], pre[:, 3:], "bf16", act)
