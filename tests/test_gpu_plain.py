@@ -232,3 +232,19 @@ def test_extreme_aspect_ratios_bit_exact(h, M, N, K):
     if K > 1 << 16:
         A = (A.float() / 8).to(A.dtype)           # |C| <= 9K/8 < 2^24 * 2^-3: exact in FP32
     assert_bit_exact(_run(h, A, B), oracle_c64(A, B, "bf16"), "bf16")
+
+
+# ---------------------------------------------------------------- FP16 shape grid (A ~ N(0,1)/sqrt(K), B ~ N(0,1))
+
+@pytest.mark.parametrize("M,N,K", [(16384, 16384, 16384), (12288, 16384, 64), (64, 12288, 16384),
+                                   (16384, 64, 12288), (8192, 12288, 4096)])
+def test_fp16_grid_shapes_sampled_rows(h, M, N, K):
+    """FP16 grid workload at its largest extents, in the launch configuration the grid times
+    (algo auto), against the oracle on 64 sampled rows."""
+    A = synthetic.matrix(M, K, "normal", 1003, "f16", "cuda", scale=1.0 / K ** 0.5)
+    B = synthetic.matrix(N, K, "normal", 2003, "f16", "cuda")
+    C = h.run(A, B, algo="auto")
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    rows = synthetic.row_sample(M, 64)
+    assert_close(C, oracle_c64(A, B, "f16", rows=rows), "f16", "plain", rows=rows)
