@@ -94,7 +94,7 @@ def test_square_2048_full(h, algo):
     assert_close(_run(h, A, B, algo), oracle_c64(A, B, "bf16"), "bf16", algo)
 
 
-@pytest.mark.parametrize("n", [4096, 8192])
+@pytest.mark.parametrize("n", [4096, 8192, 16384])
 @pytest.mark.parametrize("algo", ["strassen1", "strassen2"])
 def test_square_sampled_rows(h, n, algo):
     A, B = synthetic.operands(n, n, n, "normal", 2, "bf16", "cuda")
