@@ -458,9 +458,47 @@ def _time_launch(h, A, B, C, algo, reps, flush):
     return ts[len(ts) // 2]
 
 
+def _time_offline(h, A, B, C, algo, reps):
+    """Median device time (s) of `reps` back-to-back launches (no flush, no host gaps)."""
+    import torch
+    for _ in range(2):
+        h.run(A, B, C, algo=algo)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda._sleep(HOST_COVER_CYCLES)
+    for e0, e1 in evs:
+        e0.record()
+        h.run(A, B, C, algo=algo)
+        e1.record()
+    torch.cuda.synchronize()
+    ts = sorted(e0.elapsed_time(e1) * 1e-3 for e0, e1 in evs)
+    return ts[len(ts) // 2]
+
+
+def _time_server(h, A, B, C, algo, reps, rng):
+    """Median device time (s) of `reps` launches, each after a host pause drawn uniform in 0-5 ms."""
+    import torch
+    for _ in range(2):
+        h.run(A, B, C, algo=algo)
+    ts = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        time.sleep(float(rng.uniform(0.0, 5e-3)))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        h.run(A, B, C, algo=algo)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
 def run_grid(args):
     """Cost-model accuracy on the FP16 shape grid: time every eligible algorithm per
-    (M, N, K), check that `auto`'s choice is within 2 % of the fastest one."""
+    (M, N, K), check that `auto`'s choice is within 2 % of the fastest one.  Timing modes:
+    `flushed` (L2 flushed before each launch), `offline` (back-to-back launches), `server`
+    (seeded uniform 0-5 ms host pauses before each launch)."""
+    import numpy as np
     import torch
 
     import complexity_matmul_gb300 as lcg
@@ -469,6 +507,7 @@ def run_grid(args):
     dev = torch.device("cuda", 0)
     h = lcg.Handle(0)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    rng = np.random.default_rng(4321)
     rows, correct = [], 0
     for (M, N, K) in triples:
         A = synthetic.matrix(M, K, "normal", 1003, "f16", str(dev), scale=1.0 / K ** 0.5)
@@ -480,7 +519,12 @@ def run_grid(args):
                 h.estimate(M, N, K, lcg.F16, algo)
             except lcg.LcgemmError:
                 continue
-            times[algo] = _time_launch(h, A, B, C, algo, args.grid_reps, flush)
+            if args.grid_mode == "offline":
+                times[algo] = _time_offline(h, A, B, C, algo, args.grid_reps)
+            elif args.grid_mode == "server":
+                times[algo] = _time_server(h, A, B, C, algo, args.grid_reps, rng)
+            else:
+                times[algo] = _time_launch(h, A, B, C, algo, args.grid_reps, flush)
         chosen = lcg.ALGO_NAMES[h.select(M, N, K, lcg.F16)]
         best = min(times, key=times.get)
         ok = times[chosen] <= 1.02 * times[best]
@@ -491,7 +535,7 @@ def run_grid(args):
                      "ms": {a: round(t * 1e3, 4) for a, t in times.items()}})
         del A, B, C
     rc = h.sync_status()
-    summary = {"grid": args.grid, "shapes": len(triples), "auto_within_2pct": correct,
+    summary = {"grid": args.grid, "mode": args.grid_mode, "shapes": len(triples), "auto_within_2pct": correct,
                "fraction": round(correct / len(triples), 4), "status": rc,
                "fastest_counts": {a: sum(r["best"] == a for r in rows) for a in ("plain", "strassen1", "strassen2")}}
     print(json.dumps(summary), flush=True)
@@ -664,6 +708,8 @@ def main():
     ap.add_argument("--grid", choices=["quick", "full"], default=None,
                     help="cost-model accuracy on the FP16 shape grid (100-triple subset or all 1000)")
     ap.add_argument("--grid-out", default=None, help="--grid: write per-shape results to this JSON file")
+    ap.add_argument("--grid-mode", choices=["flushed", "offline", "server"], default="flushed",
+                    help="--grid timing: L2 flushed before each launch, back-to-back, or random 0-5 ms gaps")
     ap.add_argument("--grid-reps", type=int, default=5, help="--grid/--skinny: timed launches per algorithm")
     ap.add_argument("--skinny", action="store_true", help="time the LLM-shaped skinny GEMMs")
     ap.add_argument("--large", action="store_true",

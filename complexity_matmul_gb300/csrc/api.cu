@@ -325,9 +325,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     const int P = grid_cap(h) / 2;
     const int full = a.num_tiles / P, rem = a.num_tiles - full * P;
     const int num_kb = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
-    // the hand-off of the halves (partials through L2, a counter, the later half's
-    // sum) costs ~10 us, which only long tiles win back: split only for K >= 8192
-    const bool split = h->split && rem > 0 && 2 * rem <= P && num_kb >= 128;
+    const bool split = h->split && rem > 0 && 2 * rem <= P && num_kb >= kTailSplitMinSlabs;
     a.tail_first = split ? full * P : a.num_tiles;
     a.num_items = split ? full * P + 2 * rem : a.num_tiles;
     if (split) {
@@ -345,7 +343,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   }
   L.grid = static_cast<int>(std::min<int64_t>(tiles * a.splits, grid_cap(h)));
   if (launch_plain(L, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
-  if (a.reduce_separately && launch_splitk_reduce(L, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  if (a.reduce_separately && launch_splitk_reduce(L, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
   return LCGEMM_OK;
 }
 

@@ -230,21 +230,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
       } else {
-        // tail tile: publish this K half's FP32 partial, free the accumulator, and
+        // tail tile: publish this K half's FP32 partial (column-major slot of both
+        // ranks' 256 rows: one cache line per warp store), free the accumulator, and
         // let the second half to arrive (per tile, CTA rank and lane quarter) sum both
         const int i = tile - args.tail_first;
-        const int64_t slot_rows = int64_t(2) * kBM;   // per half: both ranks' 128 rows
-        float* mine = args.partial + ((int64_t(i) * 2 + half) * slot_rows + rank * kBM + q * 32 + lane) * kBN;
+        const int slot_rows = 2 * kBM;
+        const int64_t slot = int64_t(slot_rows) * kBN;
+        const int chunks = min(kBN / 32, (args.N - nb * kBN + 31) / 32);
+        const int64_t rloc = rank * kBM + q * 32 + lane;
+        float* mine = args.partial + (int64_t(i) * 2 + half) * slot + rloc;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < chunks; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + c * 32, r);
           tmem_wait_ld();
-          if (row < args.M) {
-            uint4* dst = reinterpret_cast<uint4*>(mine + c * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-          }
+          if (row < args.M) publish_partial(mine + c * 32 * slot_rows, slot_rows, r);
         }
         tc_fence_before();
         __syncwarp();
@@ -258,24 +258,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (prev == 1) {
           if (lane == 0) *ctr = 0;
           __threadfence();
-          const float* p0 = args.partial + ((int64_t(i) * 2) * slot_rows + rank * kBM + q * 32 + lane) * kBN;
-          const float* p1 = p0 + slot_rows * kBN;
+          const float* first = args.partial + int64_t(i) * 2 * slot + rloc;
+          if (row < args.M) {
 #pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            if (row >= args.M) break;
-            EpiLoads<32> pre;
-            if constexpr (EPI) load_chunk(row, nb * kBN + c * 32, args, pre);
-            uint32_t r[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(p0 + c * 32) + v);
-              const float4 y = __ldcg(reinterpret_cast<const float4*>(p1 + c * 32) + v);
-              r[4 * v] = __float_as_uint(x.x + y.x);
-              r[4 * v + 1] = __float_as_uint(x.y + y.y);
-              r[4 * v + 2] = __float_as_uint(x.z + y.z);
-              r[4 * v + 3] = __float_as_uint(x.w + y.w);
+            for (int c = 0; c < chunks; ++c) {
+              EpiLoads<32> pre;
+              if constexpr (EPI) load_chunk(row, nb * kBN + c * 32, args, pre);
+              uint32_t r[32];
+              sum_partials<2>(first + c * 32 * slot_rows, slot_rows, slot, r);
+              store_chunk<BF16, EPI>(crow, row, nb * kBN + c * 32, r, args, &pre);
             }
-            store_chunk<BF16, EPI>(crow, row, nb * kBN + c * 32, r, args, &pre);
           }
         }
       }

@@ -204,18 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       } else {
-        // split-K: publish this chunk's FP32 partial (rows inside C only), free TMEM
-        float* mine = args.partial + ((static_cast<int64_t>(tile) * args.splits + split) * kBM + q * 32 + lane) * BN;
+        // split-K: publish this chunk's FP32 partial (rows and column chunks inside C
+        // only; column-major slot, one cache line per warp store), free TMEM
+        const int64_t slot = int64_t(kBM) * BN;
+        const int chunks = min(BN / 32, (args.N - nb * BN + 31) / 32);
+        float* mine = args.partial + (static_cast<int64_t>(tile) * args.splits + split) * slot + q * 32 + lane;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < chunks; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tbase + c * 32, r);
           tmem_wait_ld();
-          if (row < args.M) {
-            uint4* dst = reinterpret_cast<uint4*>(mine + c * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-          }
+          if (row < args.M) publish_partial(mine + c * 32 * kBM, kBM, r);
         }
         tc_fence_before();
         __syncwarp();
@@ -235,40 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (prev == args.splits - 1) {
           if (lane == 0) args.counters[tile * 4 + q] = 0;   // ready for the next launch
           __threadfence();
-          // The quarter's valid rows x column chunks are spread over all 32 lanes,
-          // rows first, so that a skinny tile (a few valid rows) still keeps the
-          // whole warp busy; every unit sums the chunks' partials in chunk order.
-          const int rows_q = min(32, args.M - (mb * kBM + q * 32));
-          const int chunks = min(BN / 32, (args.N - nb * BN + 31) / 32);
-          const int units = rows_q > 0 ? rows_q * chunks : 0;
-          const float* qbase = args.partial + (static_cast<int64_t>(tile) * args.splits * kBM + q * 32) * BN;
+          const float* first = args.partial + static_cast<int64_t>(tile) * args.splits * slot + q * 32 + lane;
+          if (row < args.M) {
 #pragma unroll 1
-          for (int u = lane; u < units; u += 32) {
-            const int rl = u % rows_q, c = u / rows_q;
-            const int urow = mb * kBM + q * 32 + rl;
-            EpiLoads<32> pre;
-            if constexpr (EPI) load_chunk(urow, nb * BN + c * 32, args, pre);
-            float acc32[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc32[j] = 0.f;
-#pragma unroll 2
-            for (int sp = 0; sp < args.splits; ++sp) {
-              const float4* src =
-                  reinterpret_cast<const float4*>(qbase + (static_cast<int64_t>(sp) * kBM + rl) * BN + c * 32);
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 x = __ldcg(src + v);
-                acc32[4 * v] += x.x;
-                acc32[4 * v + 1] += x.y;
-                acc32[4 * v + 2] += x.z;
-                acc32[4 * v + 3] += x.w;
-              }
+            for (int c = 0; c < chunks; ++c) {
+              EpiLoads<32> pre;
+              if constexpr (EPI) load_chunk(row, nb * BN + c * 32, args, pre);
+              uint32_t r[32];
+              if (args.splits == 2) sum_partials<2>(first + c * 32 * kBM, kBM, slot, r);
+              else sum_partials<3>(first + c * 32 * kBM, kBM, slot, r);
+              store_chunk<BF16, EPI>(crow, row, nb * BN + c * 32, r, args, &pre);
             }
-            uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc32[j]);
-            store_chunk<BF16, EPI>(Cp + static_cast<int64_t>(urow) * args.ldc, urow, nb * BN + c * 32, r, args,
-                                       &pre);
           }
         }
       }
@@ -285,36 +261,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Split-K reduction: one thread per 8 consecutive columns of one valid row of
-// a tile; the partials of its chunks are summed in chunk order (four chunks'
-// loads in flight at a time), then epilogue, one rounding, store.
+// Split-K reduction: one block per (tile, 32-column chunk).  The chunk's
+// valid rows x 32 columns are dealt to the threads column-major (consecutive
+// threads on consecutive rows of a column: each load instruction reads
+// contiguous bytes of a column-major slot), so a skinny tile keeps every thread
+// busy.  Each thread sums its elements over the K chunks in chunk order, four
+// chunks' loads in flight at a time; the block transposes the sums through
+// shared memory and each thread then finishes 8-column runs of a row:
+// epilogue, one rounding, 16-byte stores.
+constexpr int kReduceThreads = 256;
+constexpr int kReducePer = 32 * kBM / kReduceThreads;   // elements per thread (full tile)
+
 template <int BN, bool BF16>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const PlainArgs a) {
-  const int64_t vec_per_row = BN / 8;
-  const int64_t total = int64_t(a.num_tiles) * kBM * vec_per_row;
-  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
-    const int tile = static_cast<int>(v / (kBM * vec_per_row));
-    const int64_t rem = v - int64_t(tile) * kBM * vec_per_row;
-    const int r = static_cast<int>(rem / vec_per_row);
-    const int c8 = static_cast<int>(rem - int64_t(r) * vec_per_row) * 8;
-    int mb, nb;
-    tile_coords(tile, a, mb, nb);
-    const int64_t row = int64_t(mb) * kBM + r;
-    const int64_t col = int64_t(nb) * BN + c8;
-    if (row >= a.M || col >= a.N) continue;
-    const float* p = a.partial + (int64_t(tile) * a.splits * kBM + r) * BN + c8;
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float4* q = reinterpret_cast<const float4*>(p + int64_t(sp) * kBM * BN);
-      const float4 x = __ldcg(q), y = __ldcg(q + 1);
-      s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
-      s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
-    }
+__global__ void __launch_bounds__(kReduceThreads) splitk_reduce_kernel(const PlainArgs a) {
+  __shared__ float T[32][kBM + 1];
+  constexpr int kChunks = BN / 32;
+  const int tile = blockIdx.x / kChunks;
+  const int c32 = (blockIdx.x % kChunks) * 32;
+  int mb, nb;
+  tile_coords(tile, a, mb, nb);
+  const int64_t row0 = int64_t(mb) * kBM;
+  const int64_t col0 = int64_t(nb) * BN + c32;
+  if (col0 >= a.N) return;                      // the whole block: no barrier skipped by part of it
+  const int rows = static_cast<int>(a.M - row0 < kBM ? a.M - row0 : kBM);
+  const int64_t slot = int64_t(kBM) * BN;
+  const float* base = a.partial + int64_t(tile) * a.splits * slot + int64_t(c32) * kBM;
+  int off[kReducePer];
+  bool on[kReducePer];
+  float s[kReducePer];
+#pragma unroll
+  for (int k = 0; k < kReducePer; ++k) {
+    const int e = threadIdx.x + k * kReduceThreads;
+    const int j = e / rows;
+    on[k] = j < 32;
+    off[k] = j * kBM + (e - j * rows);
+    s[k] = 0.f;
+  }
+#pragma unroll 1
+  for (int sp0 = 0; sp0 < a.splits; sp0 += 4) {
+    const int n = a.splits - sp0 < 4 ? a.splits - sp0 : 4;
+    float x[4][kReducePer];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < kReducePer; ++k)
+        x[i][k] = (i < n && on[k]) ? __ldcg(base + (sp0 + i) * slot + off[k]) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < kReducePer; ++k)
+        if (i < n) s[k] += x[i][k];
+  }
+#pragma unroll
+  for (int k = 0; k < kReducePer; ++k)
+    if (on[k]) T[off[k] / kBM][off[k] % kBM] = s[k];
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int u = threadIdx.x + k * kReduceThreads;     // 128 rows x 4 runs of 8 columns
+    const int rr = u / 4, c8 = (u % 4) * 8;
+    const int64_t row = row0 + rr, col = col0 + c8;
+    if (rr >= rows || col >= a.N) continue;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = T[c8 + i][rr];
     const int n = static_cast<int>(a.N - col < 8 ? a.N - col : 8);
     uint16_t* C = static_cast<uint16_t*>(a.C) + row * a.ldc + col;
-    if (a.ep.on) store_run<BF16, 8>(C, row, col, n, s, a.ep);
-    else cast_store<BF16, 8>(C, n, s);
+    if (a.ep.on) store_run<BF16, 8>(C, row, col, n, v, a.ep);
+    else cast_store<BF16, 8>(C, n, v);
   }
 }
 
@@ -333,21 +347,19 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
 }
 
 template <int BN, bool BF16>
-cudaError_t launch_reduce_impl(const PlainLaunch& L, int num_sms, cudaStream_t stream) {
-  const int64_t total = int64_t(L.args.num_tiles) * kBM * (BN / 8);
-  int64_t blocks = (total + 255) / 256;
-  blocks = blocks < int64_t(num_sms) * 8 ? blocks : int64_t(num_sms) * 8;
-  splitk_reduce_kernel<BN, BF16><<<static_cast<int>(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(L.args);
+cudaError_t launch_reduce_impl(const PlainLaunch& L, cudaStream_t stream) {
+  const int64_t blocks = int64_t(L.args.num_tiles) * (BN / 32);
+  splitk_reduce_kernel<BN, BF16><<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(L.args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_splitk_reduce(const PlainLaunch& L, int num_sms, cudaStream_t stream) {
-  if (L.bn == 256) return L.bf16 ? launch_reduce_impl<256, true>(L, num_sms, stream)
-                                 : launch_reduce_impl<256, false>(L, num_sms, stream);
-  if (L.bn == 128) return L.bf16 ? launch_reduce_impl<128, true>(L, num_sms, stream)
-                                 : launch_reduce_impl<128, false>(L, num_sms, stream);
+cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream) {
+  if (L.bn == 256) return L.bf16 ? launch_reduce_impl<256, true>(L, stream)
+                                 : launch_reduce_impl<256, false>(L, stream);
+  if (L.bn == 128) return L.bf16 ? launch_reduce_impl<128, true>(L, stream)
+                                 : launch_reduce_impl<128, false>(L, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -38,11 +38,12 @@ struct PlainArgs {
   // last chunk to finish (per `counters`) sums them in chunk order and writes C.
   int splits;
   int kb_per_split;
-  float* partial;       // [num_tiles][splits][128][BN]
+  float* partial;       // [num_tiles][splits][BN][128]: column-major slots (row fastest)
   int* counters;        // [num_tiles][4], zero before the launch
   // tail split (CTA-pair kernel only): work items below tail_first are whole tiles,
   // the 2 * (num_tiles - tail_first) items after them are K halves of the last tiles
-  // (partials in `partial` as [tile][half][256][256], counters [tile][rank][4]).
+  // (partials in `partial` as [tile][half][256 columns][256 rows], row fastest;
+  // counters [tile][rank][4]).
   int tail_first;
   int num_items;
   Epilogue ep;
@@ -67,8 +68,12 @@ cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream);
 // Split-K with at least this many chunks sums them in a separate kernel.
 constexpr int kSeparateReduceSplits = 4;
 // Sum of the split-K partials of launch L in chunk order, epilogue, one rounding (after launch_plain).
-cudaError_t launch_splitk_reduce(const PlainLaunch& L, int num_sms, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream);
 // CTA-pair variant: 256 x 256 tiles per cluster of two; tensor maps use 128-row boxes for A and B.
+// Its tail split needs at least this many 64-deep K slabs: the hand-off of the
+// halves (partials through L2, a counter, the later half's sum) costs a few
+// microseconds, which only long enough tiles win back.
+constexpr int kTailSplitMinSlabs = 96;
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 
 // Skinny GEMM (M <= 256): C^T = B . A^T with 128-row blocks of B as the MMA's

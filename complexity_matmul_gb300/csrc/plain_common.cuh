@@ -42,6 +42,35 @@ __device__ __forceinline__ void load_chunk(int row, int col, const PlainArgs& ar
     pre.vb = pre.vr = false;
 }
 
+// Split-K partial sums.  A slot holds one K chunk's FP32 partial of one tile
+// column-major: element (row r, column j) at j * ld + r.  The 32 lanes of an
+// epilogue warp hold 32 consecutive rows (the tcgen05.ld 32x32b layout: lane =
+// row, register = column), so every warp-wide access below covers 128
+// contiguous bytes, one cache line, instead of 32 lines.
+// p points at (this lane's row, the first of the 32 columns) of the slot.
+__device__ __forceinline__ void publish_partial(float* p, int ld, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) __stcg(p + j * ld, __uint_as_float(r[j]));
+}
+
+// Sum of the S chunks' partials of 32 columns of one row, in chunk order
+// (slots slot_stride floats apart); all 32 x S loads are issued before the sums.
+template <int S>
+__device__ __forceinline__ void sum_partials(const float* p, int ld, int64_t slot_stride, uint32_t (&r)[32]) {
+  float x[S][32];
+#pragma unroll
+  for (int s = 0; s < S; ++s)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[s][j] = __ldcg(p + s * slot_stride + j * ld);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float a = 0.f;
+#pragma unroll
+    for (int s = 0; s < S; ++s) a += x[s][j];
+    r[j] = __float_as_uint(a);
+  }
+}
+
 __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

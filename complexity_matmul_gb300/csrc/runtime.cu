@@ -94,7 +94,7 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
       const int units = sms / 2;
       const int64_t full = tiles / units, rem = tiles - full * units;
       double eff = wave_efficiency(tiles, units);
-      if (h->split && rem > 0 && 2 * rem <= units && K >= 8192)
+      if (h->split && rem > 0 && 2 * rem <= units && cdiv(K, 64) >= kTailSplitMinSlabs)
         eff = static_cast<double>(tiles) / ((static_cast<double>(full) + 0.5) * units);
       return std::max(mnk2 / (kEtaPlainPair * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
     }

@@ -121,7 +121,10 @@ def test_llm_skinny(h, M, N, K):
 
 # ---------------------------------------------------------------- split-K (few tiles, long K)
 
-SPLITK = [(1, 4096, 14336), (16, 1000, 2048), (100, 128, 4096), (1, 128, 4096), (128, 256, 8192), (3, 24, 1024)]
+# chunks on the single-CTA kernel: 9 (separate sum), 2 (last arriver), 4, 4, 8 (separate), none,
+# 3 with a ragged last column chunk, 2 on 128-wide tiles with partial row quarters, 4 with N < 64
+SPLITK = [(1, 4096, 14336), (16, 1000, 2048), (100, 128, 4096), (1, 128, 4096), (128, 256, 8192), (3, 24, 1024),
+          (40, 300, 3072), (200, 64, 2560), (50, 40, 4160)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLITK)
@@ -141,7 +144,7 @@ def test_split_k_float(h):
 
 # ---------------------------------------------------------------- tail split of the CTA-pair kernel
 
-@pytest.mark.parametrize("M,N,K", [(4096, 4096, 8192), (4352, 2560, 8200), (2560, 4352, 9000)])
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 8192), (4352, 2560, 8200), (2560, 4352, 9000), (4352, 2560, 6200)])
 def test_tail_split_integer_bit_exact(h, M, N, K):
     """Tiles of a partial last wave run as two K halves on two pairs (summed by the later one)."""
     A, B = synthetic.operands(M, N, K, "int3", 21, "bf16", "cuda")
