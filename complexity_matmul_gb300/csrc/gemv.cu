@@ -7,7 +7,10 @@
 // (warp w takes chunks w, w + 8, ...); in a chunk, lane l reads 8 consecutive
 // elements of each of the kRows B rows (one 512-byte contiguous run per row
 // and warp) and of each A row (L1/L2 resident: A is small and shared by all
-// blocks), and accumulates the kRows x M products in FP32.  The per-lane sums
+// blocks), and accumulates the kRows x M products in FP32.  For M = 1 a block
+// owns 4 rows (twice the blocks: short B, e.g. N = 128, still reaches many
+// SMs) and two chunks' loads per warp are in flight; M = 2 and 4 keep 8 rows
+// and one chunk, which measured faster at their register counts.  The per-lane sums
 // are reduced across the warp (shuffles), then across the 8 warps (shared
 // memory, fixed order), and the epilogue is applied once per output.
 #include "epilogue.cuh"
@@ -20,8 +23,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRows = 8;          // rows of B per block
 constexpr int kChunk = 256;       // K elements per warp iteration (32 lanes x 8)
+
+template <int MT>
+struct GemvShape {
+  static constexpr int kRows = MT == 1 ? 4 : 8;     // rows of B per block
+  static constexpr int kUnroll = MT == 1 ? 2 : 1;   // K chunks in flight per warp
+};
 
 template <bool BF16>
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
@@ -49,6 +57,8 @@ __device__ __forceinline__ uint4 load8(const uint16_t* row, int64_t k, int64_t K
 
 template <int MT, bool BF16>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
+  constexpr int kRows = GemvShape<MT>::kRows;
+  constexpr int kUnroll = GemvShape<MT>::kUnroll;
   __shared__ float red[kWarps][kRows][MT];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -67,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
   for (int r = 0; r < kRows; ++r) brow[r] = B + (n0 + r < a.N ? n0 + r : a.N - 1) * a.ldb;
 
-#pragma unroll 1
+#pragma unroll kUnroll
   for (int64_t k = (static_cast<int64_t>(warp) * kChunk) + lane * 8; k < a.K; k += kWarps * kChunk) {
     uint4 braw[kRows];
 #pragma unroll
@@ -126,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 
 template <int MT, bool BF16>
 cudaError_t launch_impl(const GemvArgs& a, cudaStream_t st) {
+  constexpr int kRows = GemvShape<MT>::kRows;
   const int64_t blocks = (a.N + kRows - 1) / kRows;
   gemv_kernel<MT, BF16><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a);
   return cudaGetLastError();
