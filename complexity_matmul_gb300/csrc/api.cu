@@ -296,7 +296,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     // of at least 16 slabs so that tiles x chunks approaches the SM count.
     const int num_kb = a.kb_per_split;
     const int cap = grid_cap(h);
-    if (tiles < cap / 2 && num_kb >= 32) {
+    if (tiles < cap / 2 && num_kb >= kSplitKMinSlabs) {
       // chunks of at least 16 slabs: the fix-up's latency grows with the number of chunks
       int splits = std::min<int64_t>(cap / tiles, num_kb / 16);
       splits = std::max(1, std::min(splits, 64));

@@ -67,6 +67,10 @@ constexpr int kPlainBK = 64;
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream);
 // Split-K with at least this many chunks sums them in a separate kernel.
 constexpr int kSeparateReduceSplits = 4;
+// Split-K needs at least this many 64-deep K slabs per tile: the hand-off
+// (partials out, a counter, the sum) costs about as much as 24 slabs of a
+// single-CTA tile's main loop, so two chunks of 16 do not pay it back.
+constexpr int kSplitKMinSlabs = 48;
 // Sum of the split-K partials of launch L in chunk order, epilogue, one rounding (after launch_plain).
 cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream);
 // CTA-pair variant: 256 x 256 tiles per cluster of two; tensor maps use 128-row boxes for A and B.

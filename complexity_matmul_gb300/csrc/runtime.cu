@@ -103,7 +103,7 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
     const int64_t bn = N <= 128 ? 128 : 256;
     const int64_t tiles = cdiv(M, 128) * cdiv(N, bn), num_kb = cdiv(K, 64);
     int64_t splits = 1;
-    if (tiles < sms / 2 && num_kb >= 32) splits = std::max<int64_t>(1, std::min<int64_t>(sms / tiles, num_kb / 16));
+    if (tiles < sms / 2 && num_kb >= kSplitKMinSlabs) splits = std::max<int64_t>(1, std::min<int64_t>(sms / tiles, num_kb / 16));
     const double part_bytes = splits > 1 ? 2.0 * 4.0 * static_cast<double>(tiles * splits) * 128.0 * bn : 0.0;
     double t = kernel_time(mnk2, bytes + part_bytes, tiles * splits, sms, kEtaPlainSingle, P, BW);
     if (splits >= kSeparateReduceSplits) t += kernel_time(0, part_bytes / 2 + 2.0 * m * n, 0, 1, 1.0, P, BW);

@@ -104,6 +104,17 @@ def test_few_tile_long_k_shapes_use_split_k(plan):
     assert plan.select(M, N, K, lcg.BF16) == lcg.PLAIN
 
 
+def test_split_k_threshold_at_48_slabs(plan):
+    """Split-K starts at 48 K slabs: a 32-slab tile runs unsplit (two 16-slab chunks measured 3 us
+    slower than one CTA on GB300), while 48 slabs split into three chunks, so the longer K is
+    estimated cheaper."""
+    t32 = plan.estimate(128, 256, 2048, lcg.BF16, "plain")
+    t48 = plan.estimate(128, 256, 3072, lcg.BF16, "plain")
+    one_cta_32 = 2.0 * 128 * 256 * 2048 / (2.25e15 / 152)
+    assert t32 > one_cta_32
+    assert t48 < t32
+
+
 def test_pair_tiles_only_when_they_fill_the_pairs(plan):
     """CTA pairs need their 256 x 256 tiles to fill a quarter of the pairs; below that the estimate
     is the single-CTA split-K one, which for few tiles is lower than the pair estimate."""

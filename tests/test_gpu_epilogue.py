@@ -135,7 +135,7 @@ def test_plain_full_size_sampled_rows(h):
 # ---------------------------------------------------------------- split paths apply it once, after the sum
 
 # single-CTA chunks: 4, 4, 8 (separate sum), 2 and 3 (last arriver), 4 with N < 64
-@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 4096), (128, 512, 8192), (16, 1000, 2048),
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 4096), (128, 512, 8192), (16, 14336, 3072),
                                    (40, 300, 3072), (50, 40, 4160)])
 def test_split_k_skinny(h, M, N, K):
     _exact(h, M, N, K, "bf16", "relu")

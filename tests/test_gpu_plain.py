@@ -121,10 +121,11 @@ def test_llm_skinny(h, M, N, K):
 
 # ---------------------------------------------------------------- split-K (few tiles, long K)
 
-# chunks on the single-CTA kernel: 9 (separate sum), 2 (last arriver), 4, 4, 8 (separate), none,
-# 3 with a ragged last column chunk, 2 on 128-wide tiles with partial row quarters, 4 with N < 64
+# chunks on the single-CTA kernel: 9 (separate sum), none (32 slabs), 4, 4, 8 (separate), none,
+# 3 with a ragged last column chunk (last arriver), 3 on 128-wide tiles with partial row quarters,
+# 4 with N < 64, 2 (56 tiles: last arriver)
 SPLITK = [(1, 4096, 14336), (16, 1000, 2048), (100, 128, 4096), (1, 128, 4096), (128, 256, 8192), (3, 24, 1024),
-          (40, 300, 3072), (200, 64, 2560), (50, 40, 4160)]
+          (40, 300, 3072), (200, 64, 3200), (50, 40, 4160), (16, 14336, 3072)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLITK)
