@@ -291,6 +291,8 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   a.ep = ep;
   a.splits = 1;
   a.kb_per_split = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
+  // one tile row: each B tile is read by one CTA (per K chunk) and never again
+  a.b_read_once = (!pair && a.tiles_m == 1) ? 1 : 0;
   if (!pair) {
     // Too few tiles to fill the machine (skinny M, small N): cut K into chunks
     // of at least 16 slabs so that tiles x chunks approaches the SM count.

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
+      const uint64_t b_policy = l2_policy_evict_first();
       bool ok = true;
       for (int w = blockIdx.x; ok && w < num_work; w += gridDim.x) {
         const int tile = w / args.splits, split = w - tile * args.splits;
@@ -98,7 +99,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBK, mb * kBM);
-          tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, nb * BN);
+          if (args.b_read_once)
+            tma_load_2d_hint(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, nb * BN, b_policy);
+          else
+            tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, nb * BN);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
+      const uint64_t b_policy = l2_policy_evict_first();   // every B byte is read once
       bool ok = true;
       for (int64_t it = it_begin; ok && it < it_end;) {
         const int blk = static_cast<int>(it / S);
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < SUB; ++j) {
             const int x = (s * SUB + j) * kBK;   // boxes past K read zeros
-            tma_load_2d(sB + stage * C::kBBytes + j * C::kBBox, &tmB, &full[stage], x, blk * kRowsB);
+            tma_load_2d_hint(sB + stage * C::kBBytes + j * C::kBBox, &tmB, &full[stage], x, blk * kRowsB, b_policy);
             tma_load_2d(sA + stage * C::kABytes + j * C::kABox, &tmA, &full[stage], x, 0);
           }
           armed |= 1u << stage;

@@ -50,6 +50,9 @@ struct PlainArgs {
   // split-K with many chunks: the chunks only publish their partials and a
   // separate reduction kernel sums them (every output element in parallel)
   int reduce_separately;
+  // single-CTA kernel: every B tile is read once (one tile row): its loads
+  // carry an L2 evict-first policy
+  int b_read_once;
 };
 
 struct PlainLaunch {
