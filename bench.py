@@ -437,6 +437,8 @@ def run_case(args):
 # A device-side sleep (~0.2 ms) between the L2 flush and the timed launch: the host enqueues the
 # launch while the GPU sleeps, so no host-side gap lands between the two events of a short kernel.
 HOST_COVER_CYCLES = 400_000
+OFFLINE_REPS = 20                # --grid-mode offline: back-to-back launches per algorithm and shape
+OFFLINE_COVER_CYCLES = 4_000_000 # GPU sleep (~2 ms) covering the host's enqueueing of those launches
 
 
 def _time_launch(h, A, B, C, algo, reps, flush):
@@ -459,19 +461,20 @@ def _time_launch(h, A, B, C, algo, reps, flush):
 
 
 def _time_offline(h, A, B, C, algo, reps):
-    """Median device time (s) of `reps` back-to-back launches (no flush, no host gaps)."""
+    """Device time (s) per launch of `reps` back-to-back launches (no flush, no host gaps): one event
+    pair around all of them, since consecutive launches may overlap (a kernel's prologue runs while
+    the one before it finishes) and an event between two launches would serialise them."""
     import torch
     for _ in range(2):
         h.run(A, B, C, algo=algo)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    torch.cuda._sleep(HOST_COVER_CYCLES)
-    for e0, e1 in evs:
-        e0.record()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(OFFLINE_COVER_CYCLES)       # the host enqueues all launches before the GPU reaches them
+    e0.record()
+    for _ in range(reps):
         h.run(A, B, C, algo=algo)
-        e1.record()
+    e1.record()
     torch.cuda.synchronize()
-    ts = sorted(e0.elapsed_time(e1) * 1e-3 for e0, e1 in evs)
-    return ts[len(ts) // 2]
+    return e0.elapsed_time(e1) * 1e-3 / reps
 
 
 def _time_server(h, A, B, C, algo, reps, rng):
@@ -520,7 +523,7 @@ def run_grid(args):
             except lcg.LcgemmError:
                 continue
             if args.grid_mode == "offline":
-                times[algo] = _time_offline(h, A, B, C, algo, args.grid_reps)
+                times[algo] = _time_offline(h, A, B, C, algo, OFFLINE_REPS)
             elif args.grid_mode == "server":
                 times[algo] = _time_server(h, A, B, C, algo, args.grid_reps, rng)
             else:

@@ -179,7 +179,7 @@ int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K) {
 }
 
 int run_gemv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-             int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
+             int64_t ldc, bool bf16, const Epilogue& ep, bool pdl, cudaStream_t st) {
   GemvArgs a{};
   a.A = A;
   a.lda = lda;
@@ -191,7 +191,7 @@ int run_gemv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const 
   a.N = N;
   a.K = K;
   a.ep = ep;
-  return launch_gemv(a, bf16, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
+  return launch_gemv(a, bf16, pdl, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
 }
 
 int skinny_sub(int mp, int64_t /*K*/) { return mp <= 64 ? 4 : 2; }
@@ -200,6 +200,7 @@ int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, in
                int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
   SkinnyLaunch L{};
   L.bf16 = bf16;
+  L.pdl = h->pdl != 0;
   L.mp = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, L.mp)) return LCGEMM_ERR_CUDA;
   if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, 128)) return LCGEMM_ERR_CUDA;
@@ -265,10 +266,11 @@ int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, in
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
   const int variant = plain_variant(h, M, N, K);
-  if (variant == 4) return run_gemv(M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
+  if (variant == 4) return run_gemv(M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, h->pdl != 0, st);
   if (variant == 3) return run_skinny(h, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
   PlainLaunch L{};
   L.bf16 = bf16;
+  L.pdl = h->pdl != 0;
   const bool pair = variant == 2;
   const int bm = pair ? 2 * kPlainBM : kPlainBM;
   L.bn = pair ? 256 : (N <= 128 ? 128 : 256);

@@ -100,6 +100,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: the next kernel in the stream may start its
+  // prologue now, and no global memory is touched before the kernel before this
+  // one has completed (its writes, e.g. to A, B or C, are then visible).
+  griddep_launch_dependents();
+  griddep_wait();
   const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
   const int num_kb = (args.K + kBK - 1) / kBK;
   const int pair = blockIdx.x / 2;
@@ -293,8 +298,7 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<L.grid, kThreads, kSmemBytes, stream>>>(L.tmA, L.tmB, L.args);
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
 }
 
 }  // namespace

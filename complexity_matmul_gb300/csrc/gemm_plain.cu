@@ -77,6 +77,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: the next kernel in the stream may start its
+  // prologue now, and no global memory is touched before the kernel before this
+  // one has completed (its writes, e.g. to A, B or C, are then visible).
+  griddep_launch_dependents();
+  griddep_wait();
   const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
   const int num_kb = (args.K + kBK - 1) / kBK;
   const int num_work = args.num_tiles * args.splits;
@@ -346,8 +351,7 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tmA, L.tmB, L.args);
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, L.grid, kThreads, C::kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
 }
 
 template <int BN, bool BF16>

@@ -203,6 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: the next kernel in the stream may start its
+  // prologue now, and no global memory is touched before the kernel before this
+  // one has completed (its writes, e.g. to A, B or C, are then visible).
+  griddep_launch_dependents();
+  griddep_wait();
   const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
   const int64_t it_begin = range_begin(cta, args.total, grid);
   const int64_t it_end = range_begin(cta + 1, args.total, grid);
@@ -385,8 +390,7 @@ cudaError_t launch_impl(const SkinnyLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<L.grid, kThreads, C::kSmemBytes, stream>>>(L.tmA, L.tmB, L.args);
-  return cudaGetLastError();
+  return launch_maybe_pdl(kern, L.grid, kThreads, C::kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
   }
 }
 

@@ -60,6 +60,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   constexpr int kRows = GemvShape<MT>::kRows;
   constexpr int kUnroll = GemvShape<MT>::kUnroll;
   __shared__ float red[kWarps][kRows][MT];
+  // Programmatic dependent launch: let the next kernel be scheduled, then wait
+  // for the kernel before this one (A, B or C may be its output).
+  griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kRows;
@@ -135,25 +139,24 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 }
 
 template <int MT, bool BF16>
-cudaError_t launch_impl(const GemvArgs& a, cudaStream_t st) {
+cudaError_t launch_impl(const GemvArgs& a, bool pdl, cudaStream_t st) {
   constexpr int kRows = GemvShape<MT>::kRows;
   const int64_t blocks = (a.N + kRows - 1) / kRows;
-  gemv_kernel<MT, BF16><<<static_cast<unsigned>(blocks), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_maybe_pdl(gemv_kernel<MT, BF16>, static_cast<int>(blocks), kThreads, 0, st, pdl, a);
 }
 
 template <bool BF16>
-cudaError_t launch_m(const GemvArgs& a, cudaStream_t st) {
-  if (a.M <= 1) return launch_impl<1, BF16>(a, st);
-  if (a.M <= 2) return launch_impl<2, BF16>(a, st);
-  return launch_impl<4, BF16>(a, st);
+cudaError_t launch_m(const GemvArgs& a, bool pdl, cudaStream_t st) {
+  if (a.M <= 1) return launch_impl<1, BF16>(a, pdl, st);
+  if (a.M <= 2) return launch_impl<2, BF16>(a, pdl, st);
+  return launch_impl<4, BF16>(a, pdl, st);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st) {
+cudaError_t launch_gemv(const GemvArgs& a, bool bf16, bool pdl, cudaStream_t st) {
   if (a.M < 1 || a.M > kGemvMaxM) return cudaErrorInvalidValue;
-  return bf16 ? launch_m<true>(a, st) : launch_m<false>(a, st);
+  return bf16 ? launch_m<true>(a, pdl, st) : launch_m<false>(a, pdl, st);
 }
 
 }  // namespace lcg

@@ -61,6 +61,7 @@ struct PlainLaunch {
   int bn;               // 128 or 256
   bool bf16;
   int grid;
+  bool pdl;             // launch as a programmatic dependent of the kernel before it
 };
 
 // Box sizes the plain kernel expects in its tensor maps.
@@ -111,6 +112,7 @@ struct SkinnyLaunch {
   int sub;                         // 64-deep K boxes per pipeline stage: 4 for mp <= 64, else 2
   bool bf16;
   int grid;
+  bool pdl;                        // launch as a programmatic dependent of the kernel before it
 };
 cudaError_t launch_skinny(const SkinnyLaunch& L, cudaStream_t stream);
 constexpr int kSkinnyMaxM = 256;
@@ -129,7 +131,7 @@ struct GemvArgs {
   Epilogue ep;
 };
 constexpr int kGemvMaxM = 4;
-cudaError_t launch_gemv(const GemvArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_gemv(const GemvArgs& a, bool bf16, bool pdl, cudaStream_t st);
 
 // ---------------------------------------------------------------- LCMA pre-pass / recombination
 

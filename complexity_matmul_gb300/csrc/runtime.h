@@ -19,7 +19,7 @@ struct lcgemm_ctx {
   int debug_drop = 0;
   int plain_kernel = 0;         // 0: choose, 1: single-CTA 128 x 256 tiles, 2: CTA-pair 256 x 256 tiles,
                                 // 3: skinny (M <= 256; larger M choose), 4: CUDA-core GEMV (M <= 4)
-  int pdl = 1;                  // launch LCMA kernels as programmatic dependents of the kernel before them
+  int pdl = 1;                  // launch GEMM kernels as programmatic dependents of the kernel before them
   int lcma_kernel = 0;          // fused one-level: 0 choose, 1 single-CTA 128 x 128 Groups, 2 CTA-pair 256 x 128
   double peak_gflops = 2.25e6;  // dense FP16/BF16 tensor peak (GFLOP/s)
   double hbm_gbps = 8000.0;     // HBM bandwidth (GB/s)

@@ -116,9 +116,11 @@ enum {
                                       (M <= 4); for 3 and 4 larger M choose                            */
   LCGEMM_OPT_LCMA_KERNEL = 9,       /* fused one-level Strassen kernel: 0 choose (default), 1
                                       single-CTA 128x128 Groups, 2 CTA-pair 256x128 Groups           */
-  LCGEMM_OPT_PDL = 10               /* 1: launch the Strassen product kernel as a programmatic
-                                      dependent of the pre-pass (its prologue overlaps the pre-pass
-                                      tail; default), 0: plain stream order                           */
+  LCGEMM_OPT_PDL = 10               /* 1 (default): launch the GEMM kernels (plain tiles, GEMV,
+                                      skinny, Strassen products) as programmatic dependents of the
+                                      kernel before them: their prologue (barriers, tensor memory,
+                                      descriptors) overlaps that kernel's tail and they touch no
+                                      global memory before it completes; 0: plain stream order     */
 };
 
 /* `device` value of a planning handle (see lcgemm_create). */
