@@ -296,8 +296,10 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   // one tile row: each B tile is read by one CTA (per K chunk) and never again
   a.b_read_once = (!pair && a.tiles_m == 1) ? 1 : 0;
   if (!pair) {
-    // Too few tiles to fill the machine (skinny M, small N): cut K into chunks
-    // of at least 16 slabs so that tiles x chunks approaches the SM count.
+    // Too few tiles to fill the machine (skinny M, small N) and a long enough K
+    // (kSplitKMinSlabs): cut K into chunks of at least 16 slabs so that
+    // tiles x chunks approaches the SM count.  Rounding the chunk length up
+    // never raises the chunk count, so the last arriver sums two or three.
     const int num_kb = a.kb_per_split;
     const int cap = grid_cap(h);
     if (tiles < cap / 2 && num_kb >= kSplitKMinSlabs) {

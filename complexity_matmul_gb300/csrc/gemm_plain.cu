@@ -9,6 +9,12 @@
 //   warps 2..5  epilogue: tcgen05.ld -> cvt.rn -> global stores, overlapped
 //               with the next tile's main loop through the second accumulator
 //
+// Few tiles and a long K: the launcher cuts each tile's K range into chunks
+// (split-K) on consecutive work items; a chunk's FP32 partial goes to a
+// column-major slot of the workspace, and two or three chunks are summed by
+// the last to arrive, more by splitk_reduce_kernel.  When C has one tile row,
+// every B tile is read once and its loads carry an L2 evict-first policy.
+//
 // Prior art for the tiling, the multi-stage prefetch and the block swizzle:
 // CUDA-L2 summary (gist.science 2512.02551), "discovered techniques" list
 // (double-buffering, multi-step prefetch, block swizzling for L2 hit rate).
@@ -23,6 +29,7 @@ namespace {
 constexpr int kBM = kPlainBM;
 constexpr int kBK = kPlainBK;
 constexpr int kThreads = 192;
+static_assert(kSeparateReduceSplits == 4, "the last arriver's sum is instantiated for 2 and 3 chunks");
 
 template <int BN, int STAGES>
 struct Cfg {
