@@ -68,6 +68,15 @@ def test_wave_quantisation():
     h.close()
 
 
+def test_tail_split_from_96_slabs(plan):
+    """The partial last wave runs as K halves from 96 K slabs (K = 6144): 80 tiles then cost about
+    one and a half waves; with 64 slabs (K = 4096) the hand-off does not pay and they cost two."""
+    def ratio(K):
+        return plan.estimate(1024, 256 * 20, K, lcg.BF16, "plain") / plan.estimate(1024, 256 * 19, K, lcg.BF16, "plain")
+    assert ratio(6144) < 1.7
+    assert ratio(4096) > 1.7
+
+
 def test_strassen_saves_multiplies_only_when_large(plan):
     # small shapes: the pre-pass and launches dominate, plain wins
     for n in (256, 1024, 2048):
