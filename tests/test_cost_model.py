@@ -115,13 +115,11 @@ def test_few_tile_long_k_shapes_use_split_k(plan):
 
 def test_split_k_threshold_at_48_slabs(plan):
     """Split-K starts at 48 K slabs: a 32-slab tile runs unsplit (two 16-slab chunks measured 3 us
-    slower than one CTA on GB300), while 48 slabs split into three chunks, so the longer K is
-    estimated cheaper."""
-    t32 = plan.estimate(128, 256, 2048, lcg.BF16, "plain")
-    t48 = plan.estimate(128, 256, 3072, lcg.BF16, "plain")
-    one_cta_32 = 2.0 * 128 * 256 * 2048 / (2.25e15 / 152)
-    assert t32 > one_cta_32
-    assert t48 < t32
+    slower than one CTA on GB300), while 48 slabs split into three chunks, so at M = 16 (chunks
+    summed by the last to arrive, no extra launch) the longer K is estimated cheaper."""
+    t32 = plan.estimate(16, 256, 2048, lcg.BF16, "plain")
+    t48 = plan.estimate(16, 256, 3072, lcg.BF16, "plain")
+    assert t48 < t32      # were 32 slabs split too, both would run 16-slab chunks
 
 
 def test_pair_tiles_only_when_they_fill_the_pairs(plan):
