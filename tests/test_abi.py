@@ -93,3 +93,30 @@ def test_epilogue_entry_rejects_planning_and_null_handles(library):
     h = lcg.Handle(lcg.PLANNING_DEVICE)
     assert h.run_epilogue_raw(8, 8, 8, None, 8, None, 8, None, 8, lcg.BF16, lcg.PLAIN, act="relu") == lcg.ERR_ARG
     h.close()
+
+
+@pytest.mark.parametrize("option,bad", [(lcg.OPT_WAIT_TIMEOUT_US, 0), (lcg.OPT_WAIT_TIMEOUT_US, 61_000_000),
+                                        (lcg.OPT_GROUP_ORDER, 2), (lcg.OPT_SPLIT, -1), (lcg.OPT_MAX_CTAS, -1),
+                                        (lcg.OPT_PEAK_GFLOPS, 0), (lcg.OPT_HBM_GBPS, -5),
+                                        (lcg.OPT_DEBUG_DROP_SIGNAL, 3), (lcg.OPT_PLAIN_KERNEL, 5),
+                                        (lcg.OPT_LCMA_KERNEL, 3), (lcg.OPT_PDL, 2), (999, 1)])
+def test_set_option_rejects_bad_values(option, bad):
+    """Every option checks its range (and unknown keys are refused) with LCGEMM_ERR_ARG, on a
+    planning handle, without a GPU."""
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    try:
+        rc = h._lib.lcgemm_set_option(h._h, option, bad)
+        assert rc == lcg.ERR_ARG
+    finally:
+        h.close()
+
+
+def test_set_option_accepts_valid_values():
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    try:
+        for option, good in [(lcg.OPT_WAIT_TIMEOUT_US, 1000), (lcg.OPT_GROUP_ORDER, 0), (lcg.OPT_SPLIT, 1),
+                             (lcg.OPT_MAX_CTAS, 76), (lcg.OPT_PEAK_GFLOPS, 1951800), (lcg.OPT_HBM_GBPS, 6700),
+                             (lcg.OPT_PLAIN_KERNEL, 4), (lcg.OPT_LCMA_KERNEL, 2), (lcg.OPT_PDL, 0)]:
+            assert h._lib.lcgemm_set_option(h._h, option, good) == lcg.OK
+    finally:
+        h.close()
