@@ -120,7 +120,12 @@ enum {
                                       skinny, Strassen products) as programmatic dependents of the
                                       kernel before them: their prologue (barriers, tensor memory,
                                       descriptors) overlaps that kernel's tail and they touch no
-                                      global memory before it completes; 0: plain stream order     */
+                                      global memory before it completes; 0: plain stream order.
+                                      The GEMM kernels let their own dependents start early: a
+                                      kernel the caller launches after a run with programmatic
+                                      stream serialization must wait for its prerequisite grid
+                                      (cudaGridDependencySynchronize) before reading C; ordinary
+                                      launches, copies and events are ordered as usual.            */
 };
 
 /* `device` value of a planning handle (see lcgemm_create). */
