@@ -622,6 +622,13 @@ int lcgemm_estimate(lcgemm_t h, int64_t M, int64_t N, int64_t K, int dtype, int 
   if (!h || !seconds) return LCGEMM_ERR_ARG;
   int rc = check_shape(M, N, K, dtype, algo);
   if (rc) return rc;
+  // mirror lcgemm_run's early exits: an empty C launches nothing, and with K = 0
+  // C is only filled (or the epilogue applied), whatever algorithm was asked for
+  if (M == 0 || N == 0) {
+    *seconds = 0.0;
+    return LCGEMM_OK;
+  }
+  if (K == 0) algo = LCGEMM_PLAIN;
   if (algo == LCGEMM_AUTO) algo = select_algo(h, M, N, K, dtype);
   if (!algo_supported(algo, M, N, K)) return LCGEMM_ERR_UNSUPPORTED;
   *seconds = estimate_seconds(h, algo, M, N, K);

@@ -27,8 +27,7 @@ def test_non_divisible_shapes_pay_for_padding(plan):
     assert t_odd < t_even * 1.2
     assert plan.estimate(131, 66, 48, lcg.BF16, "strassen1") > 0
     assert plan.estimate(130, 68, 64, lcg.BF16, "strassen2") > plan.estimate(132, 68, 64, lcg.BF16, "strassen2")
-    with pytest.raises(lcg.LcgemmError):
-        plan.estimate(0, 8, 8, lcg.BF16, "strassen1")
+    assert plan.estimate(0, 8, 8, lcg.BF16, "strassen1") == 0.0      # an empty C: nothing runs
 
 
 @pytest.mark.parametrize("shape", [(131, 257, 1000), (1, 4096, 4095), (4097, 4097, 4097), (64, 64, 8)])
@@ -132,3 +131,20 @@ def test_pair_tiles_only_when_they_fill_the_pairs(plan):
     t_pair = h.estimate(*shape, lcg.BF16, "plain")
     h.close()
     assert t_default < t_pair
+
+
+def test_degenerate_shapes(plan):
+    """An empty C launches nothing (estimate 0); K = 0 still writes C (a launch); negative sizes,
+    unknown dtypes and unknown algorithms are argument errors."""
+    import ctypes
+    def est(M, N, K, dtype=lcg.BF16, algo=lcg.PLAIN):
+        s = ctypes.c_double(-1.0)
+        return plan._lib.lcgemm_estimate(plan._h, M, N, K, dtype, algo, ctypes.byref(s)), s.value
+    assert est(0, 128, 128) == (lcg.OK, 0.0)
+    assert est(128, 0, 128, algo=lcg.STRASSEN2) == (lcg.OK, 0.0)
+    rc, t = est(128, 128, 0)
+    assert rc == lcg.OK and t > 0.0
+    assert est(128, 128, 0, algo=lcg.STRASSEN1) == (rc, t)        # K = 0 fills C the same way
+    assert est(-1, 128, 128)[0] == lcg.ERR_ARG
+    assert est(128, 128, 128, dtype=7)[0] == lcg.ERR_ARG
+    assert est(128, 128, 128, algo=9)[0] == lcg.ERR_ARG
