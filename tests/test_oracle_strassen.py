@@ -158,3 +158,52 @@ def test_two_level_bf16_inherent_max_error():
     m1 = np.abs(oracle.rounding.rne_values(S.strassen(Ad, Bd, 1, "emulate", 1), 1) - C64).max() / sig
     m2 = np.abs(oracle.rounding.rne_values(S.strassen(Ad, Bd, 2, "emulate", 1), 1) - C64).max() / sig
     assert m1 < 0.05 < m2 < 0.10
+
+
+def _emulate_golden():
+    cases, sums = {}, []
+    for line in open(os.path.join(GOLDEN, "strassen_emulate.txt")):
+        f = line.split("#")[0].split()
+        if not f:
+            continue
+        if f[0] == "case":
+            name = f[1]
+            cases[name] = {"levels": int(f[2]), "M": int(f[3]), "K": int(f[4]), "N": int(f[5])}
+        elif f[0] == "sum":
+            arrow = f.index("->")
+            sums.append((f[1], [float(v) for v in f[2:arrow]], float(f[arrow + 1])))
+        else:
+            cases[name][f[0]] = np.array([float(v) for v in f[1:]])
+    return cases, sums
+
+
+@pytest.mark.parametrize("name", ["one_level", "two_level_tie", "two_level_three_terms"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_emulate_golden_cases(name, dtype):
+    """Hand-worked emulated C (tests/golden/strassen_emulate.txt): the operand sums are rounded
+    once, to the input type, after an FP32 sum over the raw blocks.  Rounding to the other type
+    or after every addition changes these values."""
+    c = _emulate_golden()[0][name]
+    M, K, N = c["M"], c["K"], c["N"]
+    A = c["A"].reshape(M, K)
+    B = c["B"].reshape(K, N)
+    dt = oracle.BF16 if dtype == "bf16" else oracle.F16
+    got = S.strassen(A, B, c["levels"], "emulate", dt)
+    np.testing.assert_array_equal(got, c["C_" + dtype].reshape(M, N))
+    np.testing.assert_array_equal(S.strassen(A, B, c["levels"], "f64"), A @ B)
+
+
+def test_emulate_golden_single_sums():
+    """Step 1 alone on hand-worked term lists: FP32 sum in the listed order, one rounding."""
+    _, sums = _emulate_golden()
+    assert len(sums) == 4
+    for dtype, terms, want in sums:
+        g = 2 if len(terms) <= 4 else 4
+        coef = np.zeros((g, g), np.int64)
+        blocks = [[np.zeros((1, 1)) for _ in range(g)] for _ in range(g)]
+        for i, t in enumerate(terms):               # ascending (row, column) block order
+            coef[i // g, i % g] = 1
+            blocks[i // g][i % g] = np.full((1, 1), t)
+        dt = oracle.BF16 if dtype == "bf16" else oracle.F16
+        got = S._combine(coef, blocks, "emulate", dt)
+        assert got.shape == (1, 1) and got[0, 0] == want, (dtype, terms, got[0, 0], want)
