@@ -202,6 +202,7 @@ struct LcmaArgs {
   int* flags;                     // one counter per split Group and CTA rank (zeroed before launch)
   int debug_drop;                 // test hook: second halves never publish
   int raw2d;                      // CTA-pair path: raw-block maps are 2-D maps of the whole operand
+  int group_order;                // CTA-pair path: 1 all pairs walk one product order; 0 odd pairs another
   int64_t ldp;
   int num_products;
   int* err;

@@ -9,29 +9,35 @@
 // operand footprint per flop as the plain CTA-pair kernel, half the shared-
 // memory traffic of 128-wide product tiles, which is what limits those.
 //
-// Tensor memory holds two 256-column product accumulators (all 512 columns),
-// so product p+1 accumulates while the epilogue consumes product p.  The four
-// quadrant sums live in FP32 in a per-CTA scratch that stays in L2 (three
-// slots are enough because of the product order):
+// Tensor memory holds two 256-column accumulators (all 512 columns); the MMA
+// writes them alternately, so product p+1 runs while the epilogue consumes
+// product p.  Two products go straight onto the accumulator two steps back
+// instead of into a fresh one: M7 (negated through the instruction's negate-A
+// bit) onto M5 and M6 onto M3, so the accumulator already holds the sum that a
+// C quadrant needs.  What is left of the quadrant sums lives in FP32 in a
+// per-CTA scratch of two slots that stays in L2:
 //
-//   product  epilogue (P = the product, FP32)           slots after it
-//   M5       s0  = -P ;  s1  = P                         s0=C11 s1=C12
-//   M3       C12 = s1 + P (cast, stored) ;  s1 = P       s1=C22
-//   M7       s0 += P
-//   M1       s0 += P ;  s1 += P
-//   M4       C11 = s0 + P (stored) ;  s2 = P             s2=C21
-//   M2       C21 = s2 + P (stored) ;  s1 -= P
-//   M6       C22 = s1 + P (stored)
+//   step  MMA                 epilogue (P = the accumulator, FP32)   slots after it
+//   0     M5         -> X     s0  = P                               s0=C12
+//   1     M3         -> Y     C12 = s0 + P (cast, stored)
+//   2     X += -M7  (M5-M7)   s0  = -P                              s0=C11
+//   3     Y += M6   (M3+M6)   s1  = P                               s1=C22
+//   4     M1         -> X     s0 += P ;  s1 += P
+//   5     M4         -> Y     C11 = s0 + P (stored) ;  s0 = P       s0=C21
+//   6     M2         -> X     C21 = s0 + P (stored) ;  C22 = s1 - P (stored)
 //
-// Every quadrant is accumulated in FP32 and cast once (numerics paragraphs of
-// the write-up's "从缓存重排到 Cost Model" section).  Each epilogue thread owns
-// one accumulator row and 128 columns; the scratch is laid out column-major per
+// Twelve slot accesses per Group and CTA (six writes, six reads of 128 KB)
+// where a fresh accumulator per product needs sixteen and three slots, so the
+// scratch takes less of the L2 that the operand panels of a wave share.  Every
+// quadrant is accumulated in FP32 and cast once (numerics paragraphs of the
+// write-up's "从缓存重排到 Cost Model" section).  Each epilogue thread owns one
+// accumulator row and 128 columns; the scratch is laid out column-major per
 // slot so that a warp's 32 rows of one column are one 128-byte line.
 //
 // Cross-CTA synchronisation (as in the plain CTA-pair kernel):
 //   full[s]   leader's; armed with both CTAs' bytes; both CTAs' copies complete on it
 //   empty[s]  per CTA; the leader's MMA commit arrives on both
-//   pfull[b]  per CTA; the leader's MMA commit arrives on both when product b is done
+//   pfull[b]  per CTA; the leader's MMA commit arrives on both when accumulator b is done
 //   pempty[b] leader's; all 16 epilogue warps of the pair arrive when b is consumed
 #include "lcma_program.cuh"
 
@@ -51,81 +57,122 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTxBytes = 2 * kStageBytes;
 constexpr int kTmemCols = 2 * kTileN;
 constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
-constexpr int kSlots = 3;
+constexpr int kSlots = 2;
 constexpr int kSlotFloats = kRows * kTileN;      // one slot: 128 rows x 256 columns
 constexpr int kSteps1 = 7;
 
-// Epilogue work per product step: up to two targets.  kTgtFinalX adds the
-// partner half's partial sum (split Groups) before the cast.
-enum : int { kTgtNone = 0, kTgtInit = 1, kTgtAcc = 2, kTgtFinal = 3, kTgtFinalX = 4 };
+// Epilogue work per product step: up to two targets.
+//   kTgtInit   slot  = sign * P          kTgtAcc    slot += sign * P
+//   kTgtFinal  C     = slot + sign * P   kTgtFinalPX C    = sign * P + partner
+//   kTgtFinalSX C    = slot + partner
+// where "partner" is the same slot of the CTA that ran the other half of a
+// split Group.
+enum : int { kTgtNone = 0, kTgtInit = 1, kTgtAcc = 2, kTgtFinal = 3, kTgtFinalPX = 4, kTgtFinalSX = 5 };
 struct Target {
   int kind, slot, sign, quad;
 };
+// One product step: the product, whether its MMA accumulates onto the
+// accumulator of two steps before (same buffer: the MMA alternates between the
+// two) instead of starting it afresh, whether it negates A, and the epilogue.
 struct StepOps {
-  int product;
+  int product, onto, negate;
   Target t[2];
 };
 
 // Work item types: a whole Group, or one of the two halves of a split Group
 // (FalconGEMM write-up, "从 LCMA 到 FalconGEMM": a Group may be split over two
 // units; scheduling stays per Group, execution per tile).
-enum : int { kItemFull = 0, kItemFirst = 1, kItemSecond = 2 };
-constexpr int kItemSteps[3] = {7, 4, 3};
+// kItemFullMixed is a whole Group in another product order; with Group
+// ordering off, odd pairs run it, so that every wave mixes two product types
+// (the effect the write-up's reordering removes).
+enum : int { kItemFull = 0, kItemFirst = 1, kItemSecond = 2, kItemFullMixed = 3 };
+constexpr int kItemTypes = 4;
+constexpr int kItemSteps[kItemTypes] = {7, 4, 3, 7};
 
-#define LCG_L2_PROGRAMS                                                                                      \
-  {                                                                                                          \
-    {/* whole Group */                                                                                       \
-     {4, {{kTgtInit, 0, -1, 0}, {kTgtInit, 1, 1, 1}}},     /* M5: s0 = -M5 (C11), s1 = M5 (C12) */          \
-     {2, {{kTgtFinal, 1, 1, 1}, {kTgtInit, 1, 1, 3}}},     /* M3: C12 = s1 + M3; s1 = M3 (C22) */           \
-     {6, {{kTgtAcc, 0, 1, 0}, {kTgtNone, 0, 0, 0}}},       /* M7: s0 += M7 */                               \
-     {0, {{kTgtAcc, 0, 1, 0}, {kTgtAcc, 1, 1, 3}}},        /* M1: s0 += M1, s1 += M1 */                     \
-     {3, {{kTgtFinal, 0, 1, 0}, {kTgtInit, 2, 1, 2}}},     /* M4: C11 = s0 + M4; s2 = M4 (C21) */           \
-     {1, {{kTgtFinal, 2, 1, 2}, {kTgtAcc, 1, -1, 3}}},     /* M2: C21 = s2 + M2; s1 -= M2 */                \
-     {5, {{kTgtFinal, 1, 1, 3}, {kTgtNone, 0, 0, 0}}}},    /* M6: C22 = s1 + M6 */                          \
-    {/* first half: M5 M3 M7 M1; finishes C11 and C22 with the second half's partials */                    \
-     {4, {{kTgtInit, 0, -1, 0}, {kTgtInit, 1, 1, 1}}},                                                       \
-     {2, {{kTgtFinal, 1, 1, 1}, {kTgtInit, 1, 1, 3}}},                                                       \
-     {6, {{kTgtAcc, 0, 1, 0}, {kTgtNone, 0, 0, 0}}},                                                         \
-     {0, {{kTgtFinalX, 0, 1, 0}, {kTgtFinalX, 1, 1, 3}}},  /* C11 = s0 + M1 + p0, C22 = s1 + M1 + p1 */      \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}}},                                                       \
-    {/* second half: M4 M2 M6; finishes C21, publishes p0 = M4 (C11) and p1 = M6 - M2 (C22) */               \
-     {3, {{kTgtInit, 0, 1, 0}, {kTgtInit, 2, 1, 2}}},                                                        \
-     {1, {{kTgtFinal, 2, 1, 2}, {kTgtInit, 1, -1, 3}}},                                                      \
-     {5, {{kTgtAcc, 1, 1, 3}, {kTgtNone, 0, 0, 0}}},                                                         \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}},                                                        \
-     {0, {{kTgtNone, 0, 0, 0}, {kTgtNone, 0, 0, 0}}}},                                                       \
+#define LCG_NONE {kTgtNone, 0, 0, 0}
+#define LCG_L2_PROGRAMS                                                                                     \
+  {                                                                                                         \
+    {/* whole Group */                                                                                      \
+     {4, 0, 0, {{kTgtInit, 0, 1, 1}, LCG_NONE}},                  /* M5: s0 = M5 (C12) */                   \
+     {2, 0, 0, {{kTgtFinal, 0, 1, 1}, LCG_NONE}},                 /* M3: C12 = s0 + M3 */                   \
+     {6, 1, 1, {{kTgtInit, 0, -1, 0}, LCG_NONE}},                 /* M5 - M7: s0 = M7 - M5 (C11) */         \
+     {5, 1, 0, {{kTgtInit, 1, 1, 3}, LCG_NONE}},                  /* M3 + M6: s1 = M3 + M6 (C22) */         \
+     {0, 0, 0, {{kTgtAcc, 0, 1, 0}, {kTgtAcc, 1, 1, 3}}},         /* M1: s0 += M1, s1 += M1 */              \
+     {3, 0, 0, {{kTgtFinal, 0, 1, 0}, {kTgtInit, 0, 1, 2}}},      /* M4: C11 = s0 + M4; s0 = M4 (C21) */    \
+     {1, 0, 0, {{kTgtFinal, 0, 1, 2}, {kTgtFinal, 1, -1, 3}}}},   /* M2: C21 = s0 + M2; C22 = s1 - M2 */    \
+    {/* first half: M5 M3 M7 M6; finishes C12, and C11, C22 with the second half's partials */            \
+     {4, 0, 0, {{kTgtInit, 0, 1, 1}, LCG_NONE}},                                                            \
+     {2, 0, 0, {{kTgtFinal, 0, 1, 1}, LCG_NONE}},                                                           \
+     {6, 1, 1, {{kTgtInit, 0, -1, 0}, LCG_NONE}},                                                           \
+     {5, 1, 0, {{kTgtFinalPX, 1, 1, 3}, {kTgtFinalSX, 0, 1, 0}}}, /* C22 = M3+M6 + p1, C11 = s0 + p0 */     \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}},                                                                       \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}},                                                                       \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}}},                                                                      \
+    {/* second half: M4 M2 M1; finishes C21, publishes p0 = M4 + M1 (C11) and p1 = M1 - M2 (C22) */        \
+     {3, 0, 0, {{kTgtInit, 0, 1, 0}, {kTgtInit, 1, 1, 2}}},                                                 \
+     {1, 0, 0, {{kTgtFinal, 1, 1, 2}, {kTgtInit, 1, -1, 3}}},                                               \
+     {0, 0, 0, {{kTgtAcc, 0, 1, 0}, {kTgtAcc, 1, 1, 3}}},                                                   \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}},                                                                       \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}},                                                                       \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}},                                                                       \
+     {0, 0, 0, {LCG_NONE, LCG_NONE}}},                                                                      \
+    {/* whole Group, product order M3 M5 M6 M7 M1 M4 M2 */                                                 \
+     {2, 0, 0, {{kTgtInit, 0, 1, 1}, LCG_NONE}},                  /* M3: s0 = M3 (C12) */                   \
+     {4, 0, 0, {{kTgtFinal, 0, 1, 1}, LCG_NONE}},                 /* M5: C12 = s0 + M5 */                   \
+     {5, 1, 0, {{kTgtInit, 0, 1, 3}, LCG_NONE}},                  /* M3 + M6: s0 = M3 + M6 (C22) */         \
+     {6, 1, 1, {{kTgtInit, 1, -1, 0}, LCG_NONE}},                 /* M5 - M7: s1 = M7 - M5 (C11) */         \
+     {0, 0, 0, {{kTgtAcc, 0, 1, 3}, {kTgtAcc, 1, 1, 0}}},         /* M1: s0 += M1, s1 += M1 */              \
+     {3, 0, 0, {{kTgtFinal, 1, 1, 0}, {kTgtInit, 1, 1, 2}}},      /* M4: C11 = s1 + M4; s1 = M4 (C21) */    \
+     {1, 0, 0, {{kTgtFinal, 1, 1, 2}, {kTgtFinal, 0, -1, 3}}}},   /* M2: C21 = s1 + M2; C22 = s0 - M2 */    \
   }
-constexpr StepOps kL2Programs[3][kSteps1] = LCG_L2_PROGRAMS;
+constexpr StepOps kL2Programs[kItemTypes][kSteps1] = LCG_L2_PROGRAMS;
 
-// Every item type stores each of its quadrants once; together the two halves
-// of a split Group produce exactly C_q = sum_p W[q,p] M_p for all four.
+// Symbolic run of the programs at compile time (coefficients over M1..M7):
+// every item type stores each of its quadrants once, an accumulator is only
+// continued within the item that started it, a slot is only read after this
+// item wrote it, and together the two halves of a split Group produce exactly
+// C_q = sum_p W[q,p] M_p for all four quadrants.
 struct L2ProgramCheck {
   bool ok = true;
   constexpr void run(int type, int (&slot)[kSlots][7], int (&stored)[4][7], bool (&done)[4],
                      const int (&partner)[kSlots][7]) {
+    int acc[2][7] = {};
+    bool written[kSlots] = {};
     for (int s = 0; s < kItemSteps[type]; ++s) {
-      const int p = kL2Programs[type][s].product;
+      const StepOps& st = kL2Programs[type][s];
+      int* P = acc[s & 1];
+      if (st.onto && s < 2) ok = false;                 // continues an accumulator of another item
+      if (!st.onto)
+        for (int j = 0; j < 7; ++j) P[j] = 0;
+      P[st.product] += st.negate ? -1 : 1;
       for (int i = 0; i < 2; ++i) {
-        const Target t = kL2Programs[type][s].t[i];
+        const Target t = st.t[i];
+        const bool reads_slot = t.kind == kTgtAcc || t.kind == kTgtFinal || t.kind == kTgtFinalSX;
+        if (t.kind != kTgtNone && (t.slot < 0 || t.slot >= kSlots)) {
+          ok = false;
+          continue;
+        }
+        if (reads_slot && !written[t.slot]) ok = false;
         if (t.kind == kTgtInit) {
-          for (int j = 0; j < 7; ++j) slot[t.slot][j] = 0;
-          slot[t.slot][p] = t.sign;
+          for (int j = 0; j < 7; ++j) slot[t.slot][j] = t.sign * P[j];
+          written[t.slot] = true;
         } else if (t.kind == kTgtAcc) {
-          slot[t.slot][p] += t.sign;
-        } else if (t.kind == kTgtFinal || t.kind == kTgtFinalX) {
-          for (int j = 0; j < 7; ++j)
-            stored[t.quad][j] = slot[t.slot][j] + (t.kind == kTgtFinalX ? partner[t.slot][j] : 0);
-          stored[t.quad][p] += t.sign;
+          for (int j = 0; j < 7; ++j) slot[t.slot][j] += t.sign * P[j];
+        } else if (t.kind >= kTgtFinal) {
+          for (int j = 0; j < 7; ++j) {
+            const int from_slot = (t.kind == kTgtFinal || t.kind == kTgtFinalSX) ? slot[t.slot][j] : 0;
+            const int from_p = (t.kind == kTgtFinalSX) ? 0 : t.sign * P[j];
+            const int from_partner = (t.kind == kTgtFinalPX || t.kind == kTgtFinalSX) ? partner[t.slot][j] : 0;
+            stored[t.quad][j] = from_slot + from_p + from_partner;
+          }
           if (done[t.quad]) ok = false;
           done[t.quad] = true;
         }
       }
-      if (kL2Programs[type][s].t[0].kind == kTgtInit && kL2Programs[type][s].t[1].kind >= kTgtFinal &&
-          kL2Programs[type][s].t[0].slot == kL2Programs[type][s].t[1].slot)
+      // a step's two targets run chunk by chunk (target 0, then target 1): an Init
+      // must not precede a read of the same slot in the same step
+      if (st.t[0].kind == kTgtInit && st.t[1].kind != kTgtNone && st.t[1].kind != kTgtInit &&
+          st.t[1].kind != kTgtFinalPX && st.t[0].slot == st.t[1].slot)
         ok = false;
     }
   }
@@ -136,6 +183,17 @@ struct L2ProgramCheck {
       int stored[4][7] = {};
       bool done[4] = {false, false, false, false};
       run(kItemFull, slot, stored, done, none);
+      for (int q = 0; q < 4; ++q) {
+        if (!done[q]) ok = false;
+        for (int j = 0; j < 7; ++j)
+          if (stored[q][j] != kW1[q][j]) ok = false;
+      }
+    }
+    {
+      int slot[kSlots][7] = {};
+      int stored[4][7] = {};
+      bool done[4] = {false, false, false, false};
+      run(kItemFullMixed, slot, stored, done, none);
       for (int q = 0; q < 4; ++q) {
         if (!done[q]) ok = false;
         for (int j = 0; j < 7; ++j)
@@ -159,8 +217,8 @@ struct L2ProgramCheck {
 };
 static_assert(L2ProgramCheck{}.ok, "the L2-accumulating programs must compute C_q = sum_p W[q,p] M_p");
 
-__constant__ StepOps d_l2_programs[3][kSteps1] = LCG_L2_PROGRAMS;
-__constant__ int d_item_steps[3] = {7, 4, 3};
+__constant__ StepOps d_l2_programs[kItemTypes][kSteps1] = LCG_L2_PROGRAMS;
+__constant__ int d_item_steps[kItemTypes] = {7, 4, 3, 7};
 
 __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -189,10 +247,13 @@ __device__ __forceinline__ bool wait_flag(const int* flag, int target, const Wai
 }
 
 // Work item w of this launch -> Group index and item type.
-__device__ __forceinline__ void item_of(int w, const LcmaArgs& a, int& group, int& type) {
+// With Group ordering on, every pair walks its whole Groups in one product
+// order, so the pairs of a wave stream one product's operand panels at a time;
+// off, the odd pairs (w % num_pairs) take the other order.
+__device__ __forceinline__ void item_of(int w, const LcmaArgs& a, int num_pairs, int& group, int& type) {
   if (w < a.split_first) {
     group = w;
-    type = kItemFull;
+    type = (!a.group_order && ((w % num_pairs) & 1)) ? kItemFullMixed : kItemFull;
   } else {
     const int i = (w - a.split_first) >> 1;
     group = a.split_first + i;
@@ -259,9 +320,17 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
         for (int j = 0; j < 32; ++j) sp[j * kRows] = v[j] + sg * __uint_as_float(r[j]);
       } else {
         float v[32];
+        if (t.kind == kTgtFinalPX) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows] + sg * __uint_as_float(r[j]);
-        if (t.kind == kTgtFinalX) {
+          for (int j = 0; j < 32; ++j) v[j] = sg * __uint_as_float(r[j]);
+        } else if (t.kind == kTgtFinalSX) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows] + sg * __uint_as_float(r[j]);
+        }
+        if (t.kind == kTgtFinalPX || t.kind == kTgtFinalSX) {
           const float* pp = partner + (static_cast<int64_t>(t.slot) * kTileN + col) * kRows + row;
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += __ldcg(pp + j * kRows);
@@ -338,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
         int grp, type;
-        item_of(w, args_in, grp, type);
+        item_of(w, args_in, num_pairs, grp, type);
         int mb, nb;
         tile_coords_l2(grp, args_in, mb, nb);
         const int nsteps = d_item_steps[type];
@@ -375,14 +444,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_f16(BF16, 2 * kRows, kTileN);
+      constexpr uint32_t idesc_pos = idesc_f16(BF16, 2 * kRows, kTileN);
+      constexpr uint32_t idesc_neg = idesc_f16(BF16, 2 * kRows, kTileN, /*negate_a=*/true);
       const uint64_t a_desc0 = sdesc_k128(smem_u32(sA));
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
       uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
       bool ok = true, issued = false;
       for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
         int grp, type;
-        item_of(w, args_in, grp, type);
+        item_of(w, args_in, num_pairs, grp, type);
         const int nsteps = d_item_steps[type];
         for (int s = 0; ok && s < nsteps; ++s) {
           if (!mbar_wait(&pempty[buf], buf_phase ^ 1, wc)) {
@@ -391,6 +461,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kTileN;
+          // continuing the accumulator of two steps before (same buffer), or starting it afresh
+          const uint32_t onto = d_l2_programs[type][s].onto;
+          const uint32_t idesc = d_l2_programs[type][s].negate ? idesc_neg : idesc_pos;
           for (int kb = 0; kb < num_kb; ++kb) {
             if (!mbar_wait(&full[stage], phase, wc)) {
               ok = false;
@@ -400,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
             const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            for (int k = 0; k < kBK / 16; ++k) mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, onto | ((kb | k) != 0));
             mma_commit_pair(&empty[stage]);
             issued = true;
             if (++stage == kStages) {
@@ -431,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
       int grp, type;
-      item_of(w, args_in, grp, type);
+      item_of(w, args_in, num_pairs, grp, type);
       int mb, nb;
       tile_coords_l2(grp, args_in, mb, nb);
       const int rloc = mb * 2 * kRows + static_cast<int>(rank) * kRows + row;   // row inside the quadrant

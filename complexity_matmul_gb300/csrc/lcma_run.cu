@@ -157,6 +157,7 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
     a.flags = split ? flags : nullptr;
     a.debug_drop = h->debug_drop;
     a.raw2d = raw2d ? 1 : 0;
+    a.group_order = h->group_order;
     ll.grid = 2 * std::min(a.num_items, P);
     if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     return LCGEMM_OK;

@@ -101,7 +101,11 @@ enum {
 /* options for lcgemm_set_option */
 enum {
   LCGEMM_OPT_WAIT_TIMEOUT_US = 1,  /* bound on every device-side wait, microseconds (default 2000000) */
-  LCGEMM_OPT_GROUP_ORDER = 2,      /* 1: order Strassen waves by product type (default), 0: off       */
+  LCGEMM_OPT_GROUP_ORDER = 2,      /* one-level Strassen on CTA pairs: 1 (default) every pair walks
+                                      its Groups' seven products in one order, so a wave streams one
+                                      product's operands at a time (only the split tail mixes);
+                                      0: odd pairs take another order, so every wave mixes two product
+                                      types (an ablation; the result is the same bit for bit)        */
   LCGEMM_OPT_SPLIT = 3,            /* 1: split tail Groups across two CTAs (default), 0: off          */
   LCGEMM_OPT_MAX_CTAS = 4,         /* cap on the persistent grid (default 0 = one CTA per SM)         */
   LCGEMM_OPT_PEAK_GFLOPS = 5,      /* cost model: dense FP16/BF16 tensor peak, GFLOP/s                */

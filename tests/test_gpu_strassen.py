@@ -294,3 +294,21 @@ def test_programmatic_dependent_launch_on_off(h, algo):
     h.set_option(lcg.OPT_PDL, 1)
     assert torch.equal(out[0], out[1])
     assert_close(out[1].cuda(), oracle_c64(A, B, "bf16"), "bf16", algo)
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 1024), (4096, 4096, 512), (8704, 8704, 256)])
+def test_group_order_on_off(hp, M, N, K):
+    """Group ordering off puts the odd CTA pairs on another product order (every wave then mixes two
+    product types): the integer result is still exact, and N(0,1) results are the same bits as with
+    ordering on (both orders form every quadrant sum in the same FP32 order)."""
+    A, B = synthetic.operands(M, N, K, "int3", 15, "bf16", "cuda")
+    rows = None if M * N <= 4096 * 4096 else synthetic.row_sample(M, 128)
+    ref = oracle_c64(A, B, "bf16", rows=rows)
+    An, Bn = synthetic.operands(M, N, K, "normal", 16, "bf16", "cuda")
+    out = {}
+    for order in (0, 1):
+        hp.set_option(lcg.OPT_GROUP_ORDER, order)
+        assert_bit_exact(_run(hp, A, B, "strassen1"), ref, "bf16", rows=rows)
+        out[order] = _run(hp, An, Bn, "strassen1").cpu()
+    hp.set_option(lcg.OPT_GROUP_ORDER, 1)
+    assert torch.equal(out[0], out[1])
