@@ -109,7 +109,7 @@ def _traffic(kernel_file: str, n: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -124,7 +124,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -141,7 +141,7 @@ class ClockSampler:
     def summary(self):
         if not self.out:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, power = [], None, set(), []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -152,14 +152,21 @@ class ClockSampler:
                 smax = float(f[2])
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for name, val in zip(names, f[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons)}
         loaded = sorted(sm)[len(sm) // 2:] if len(sm) > 4 else sm   # upper half = samples under load
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if power:
+            out["power_w"] = statistics.median(sorted(power)[len(power) // 2:])
+        return out
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -190,6 +197,9 @@ def run_gpu(args):
         A, B, C = ops[n]
         flush.fill_(1.0)                               # evict the previous launch's operands from L2
         if timed_events is not None:
+            # a device-side wait between the flush and the start event: the host submits the
+            # GEMM while the GPU waits, so no host-side gap lands inside the event pair
+            torch.cuda._sleep(HOST_COVER_CYCLES)
             timed_events[0].record(stream)
         h.run(A, B, C, algo="auto", stream=stream)
         if timed_events is not None:
@@ -224,7 +234,8 @@ def run_gpu(args):
     flops_step = sum(2.0 * n ** 3 for n in SIZES)
     value = flops_step * args.steps * world / total_s / 1e12
 
-    # ---- server mode: seeded random 0-5 ms host sleeps before every launch
+    # ---- server mode: seeded random 0-5 ms host sleeps before every launch (the GPU idles in
+    # between); each launch is event-timed on its own
     rng = np.random.default_rng(1234 + rank)
     srv = {n: [] for n in SIZES}
     for _ in range(args.server_reps):
@@ -237,12 +248,17 @@ def run_gpu(args):
             srv[n].append(e[0].elapsed_time(e[1]))
     srv_total = sum(statistics.median(srv[n]) for n in SIZES) * 1e-3
     server_value = flops_step / srv_total / 1e12
+    server_per_size = {str(n): {"median_ms": round(statistics.median(srv[n]), 4),
+                                "p10_ms": round(float(np.percentile(srv[n], 10)), 4),
+                                "p90_ms": round(float(np.percentile(srv[n], 90)), 4),
+                                "tflops": round(2.0 * n ** 3 / (statistics.median(srv[n]) * 1e-3) / 1e12, 1)}
+                       for n in SIZES}
 
     # ---- roofline of the dominant kernel (largest share of the step)
     peak_burst, peak_sust, hbm, peak_kind = _peaks()
     dom = max(SIZES, key=lambda n: statistics.median(per_n_ms[n]))
     dom_algo = chosen[dom]
-    dom_ms = statistics.mean(per_n_ms[dom])
+    dom_ms = statistics.median(per_n_ms[dom])          # the statistic per_size reports
     mma_frac = {"plain": 1.0, "strassen1": 7 / 8, "strassen2": 49 / 64}[dom_algo]
     achieved = mma_frac * 2.0 * dom ** 3 / (dom_ms * 1e-3) / 1e12
     # square shapes above 128 run the CTA-pair kernels (gemm_pair.cu, lcma_pair.cu)
@@ -251,6 +267,7 @@ def run_gpu(args):
     roofline = {"bound": "tensor", "kernel": f"{dom_algo} GEMM {dom}^3 ({kernel_file})", "achieved": round(achieved, 1),
                 "peak": peak_burst, "unit": "TFLOP/s", "frac": round(achieved / peak_burst, 4),
                 "peak_source": f"{peak_kind} bf16 burst", "traffic": traffic,
+                "duration": "median CUDA-event time of the timed launches",
                 # the dominant launches run back to back for the whole timed region (power-capped):
                 # the measured sustained figure is the other fair denominator
                 "peak_sustained": peak_sust, "frac_sustained": round(achieved / peak_sust, 4)}
@@ -269,14 +286,17 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sizes": list(SIZES), "algo": "auto",
                        "chosen": {str(n): chosen[n] for n in SIZES}, "parallelism": f"replicas x{world}",
-                       "l2": "flushed (256 MB write) before every timed launch; inputs >= 8192^3 exceed L2"},
+                       "l2": "flushed (256 MB write) before every timed launch; inputs >= 8192^3 exceed L2",
+                       "timing": "CUDA events around each launch on the launching stream; a ~0.2 ms device-side "
+                                 "wait after the flush covers the host's submission of the GEMM"},
             "pct_of_peak": round(value / world / peak_burst, 4),
             "per_size": {str(n): {"algo": chosen[n], "median_ms": round(statistics.median(per_n_ms[n]), 4),
                                   "tflops": round(2.0 * n ** 3 / (statistics.median(per_n_ms[n]) * 1e-3) / 1e12, 1),
                                   "p10_ms": round(float(np.percentile(per_n_ms[n], 10)), 4),
                                   "p90_ms": round(float(np.percentile(per_n_ms[n], 90)), 4)} for n in SIZES},
             "server": {"value": round(server_value, 2), "unit": UNIT, "reps": args.server_reps,
-                       "gaps_ms": "uniform 0-5, seeded"},
+                       "gaps_ms": "uniform 0-5, seeded", "statistic": "sum of per-size medians",
+                       "per_size": server_per_size},
             "roofline": roofline,
             "e2e": e2e,
             "gpu_launches": args.steps * sum(launches_per_gemm[chosen[n]] for n in SIZES),
@@ -538,9 +558,19 @@ def run_grid(args):
                      "ms": {a: round(t * 1e3, 4) for a, t in times.items()}})
         del A, B, C
     rc = h.sync_status()
+    ratios = {}
+    for a in ("plain", "strassen1", "strassen2"):
+        r = sorted(row["pred_ms"][a] / row["ms"][a] for row in rows if a in row["ms"] and row["ms"][a] > 0)
+        if r:
+            ratios[a] = {"geomean": round(float(np.exp(np.mean(np.log(r)))), 3),
+                         "p10": round(float(np.percentile(r, 10)), 3), "median": round(float(np.median(r)), 3),
+                         "p90": round(float(np.percentile(r, 90)), 3)}
+    misses = [{k: row[k] for k in ("M", "N", "K", "chosen", "best", "ms")} for row in rows if not row["ok"]]
     summary = {"grid": args.grid, "mode": args.grid_mode, "shapes": len(triples), "auto_within_2pct": correct,
                "fraction": round(correct / len(triples), 4), "status": rc,
-               "fastest_counts": {a: sum(r["best"] == a for r in rows) for a in ("plain", "strassen1", "strassen2")}}
+               "fastest_counts": {a: sum(r["best"] == a for r in rows) for a in ("plain", "strassen1", "strassen2")},
+               "chosen_counts": {a: sum(r["chosen"] == a for r in rows) for a in ("plain", "strassen1", "strassen2")},
+               "predicted_over_measured": ratios, "misses": misses}
     print(json.dumps(summary), flush=True)
     if args.grid_out:
         with open(args.grid_out, "w") as f:
@@ -605,6 +635,79 @@ def run_large(args):
                          "reasons": cs.get("reasons")}
         print(json.dumps({"M": M, "N": N, "K": K, **out}), flush=True)
         del A, B, C
+
+
+RACE_SHAPES = [(4096, 4096, 4096), (8192, 8192, 8192), (16384, 16384, 16384), (24576, 24576, 24576),
+               (32768, 32768, 32768), (16384, 16384, 8192), (8192, 28672, 8192), (32768, 8192, 4096)]
+
+
+def run_race(args):
+    """Plain against one-level Strassen (and two-level) per shape, in two regimes: burst (L2
+    flushed before each launch, launches interleaved across algorithms, median of --grid-reps)
+    and sustained (--race-seconds of back-to-back launches per algorithm, SM clock and board
+    power sampled meanwhile): effective TFLOP/s = 2MNK/t, TFLOP/s per median MHz, and energy per
+    GEMM (median power x time)."""
+    import torch
+
+    import complexity_matmul_gb300 as lcg
+    import synthetic
+    dev = torch.device("cuda", 0)
+    h = lcg.Handle(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    algos = args.race_algos.split(",")
+    shapes = RACE_SHAPES if not args.race_shapes else \
+        [tuple(int(x) for x in s.split("x")) * (3 if "x" not in s else 1) for s in args.race_shapes.split(",")]
+    for (M, N, K) in shapes:
+        A, B = synthetic.operands(M, N, K, "normal", 2, "bf16", str(dev))
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        flops = 2.0 * M * N * K
+        for a in algos:
+            for _ in range(2):
+                h.run(A, B, C, algo=a)
+        torch.cuda.synchronize()
+        burst = {a: [] for a in algos}
+        with ClockSampler(0) as clk:
+            for _ in range(args.grid_reps):
+                for a in algos:
+                    flush.fill_(1.0)
+                    torch.cuda._sleep(HOST_COVER_CYCLES)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    h.run(A, B, C, algo=a)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    burst[a].append(e0.elapsed_time(e1) * 1e-3)
+        out = {"M": M, "N": N, "K": K, "burst_clock": clk.summary()}
+        for a in algos:
+            t = statistics.median(burst[a])
+            out[a] = {"burst_ms": round(t * 1e3, 3), "burst_tflops": round(flops / t / 1e12, 1)}
+        for a in algos:
+            n = max(3, int(args.race_seconds / max(min(burst[a]), 1e-6)))
+            torch.cuda.synchronize()
+            with ClockSampler(0) as clk:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(n):
+                    h.run(A, B, C, algo=a)
+                e1.record()
+                torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3 / n
+            cs = clk.summary()
+            row = out[a]
+            row.update({"sustained_ms": round(t * 1e3, 3), "sustained_tflops": round(flops / t / 1e12, 1),
+                        "launches": n, "sm_mhz": cs.get("sm_mhz"), "reasons": cs.get("reasons")})
+            if cs.get("sm_mhz"):
+                row["tflops_per_mhz"] = round(flops / t / 1e12 / cs["sm_mhz"], 4)
+            if cs.get("power_w"):
+                row["power_w"] = cs["power_w"]
+                row["joules_per_gemm"] = round(cs["power_w"] * t, 3)
+        rc = h.sync_status()
+        if rc:
+            raise RuntimeError(f"device status {rc}")
+        print(json.dumps(out), flush=True)
+        del A, B, C
+        torch.cuda.empty_cache()
+    h.close()
 
 
 PADDED_SHAPES = [((8191, 8193, 8190), (8192, 8192, 8192)), ((16383, 16385, 8191), (16384, 16384, 8192))]
@@ -700,7 +803,7 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["lcgemm", "reference"], default="lcgemm")
-    ap.add_argument("--server-reps", type=int, default=5)
+    ap.add_argument("--server-reps", type=int, default=50)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--case", default=None, help="profiling mode: run one shape 'n' or 'M,N,K' --reps times")
     ap.add_argument("--algo", default="auto", help="algorithm for --case")
@@ -718,6 +821,11 @@ def main():
     ap.add_argument("--large", action="store_true",
                     help="large rectangular shapes: plain, Strassen and its ordering / split ablations")
     ap.add_argument("--group-order", type=int, default=None, help="--case: Strassen Group ordering 0/1")
+    ap.add_argument("--race", action="store_true",
+                    help="plain vs Strassen per shape: burst (flushed, interleaved) and sustained (back to back)")
+    ap.add_argument("--race-shapes", default="", help="--race: comma-separated n or MxNxK (default: built-in list)")
+    ap.add_argument("--race-algos", default="plain,strassen1", help="--race: algorithms to compare")
+    ap.add_argument("--race-seconds", type=float, default=2.0, help="--race: seconds of back-to-back launches")
     ap.add_argument("--padded", action="store_true",
                     help="Strassen on non-divisible shapes (zero-padded operands) against divisible ones")
     ap.add_argument("--epilogue", action="store_true",
@@ -735,6 +843,8 @@ def main():
         run_epilogue(args)
     elif args.large:
         run_large(args)
+    elif args.race:
+        run_race(args)
     elif args.padded:
         run_padded(args)
     elif args.impl == "reference":

@@ -32,7 +32,8 @@ ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU, "gelu_tanh": ACT_G
 
 EXPORTS = ("lcgemm_create", "lcgemm_destroy", "lcgemm_run", "lcgemm_run_host", "lcgemm_last_algo",
            "lcgemm_select", "lcgemm_estimate", "lcgemm_sync_status", "lcgemm_set_option",
-           "lcgemm_strerror", "lcgemm_strassen1_noalloc", "lcgemm_run_epilogue")
+           "lcgemm_strerror", "lcgemm_strassen1_noalloc", "lcgemm_run_epilogue", "lcgemm_noalloc_status",
+           "lcgemm_noalloc_debug_fail")
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +81,8 @@ def lib(build_if_missing: bool = False):
         L.lcgemm_sync_status.argtypes = [vp, vp]
         L.lcgemm_set_option.argtypes = [vp, i32, i64]
         L.lcgemm_strassen1_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp]
+        L.lcgemm_noalloc_status.argtypes = [vp]
+        L.lcgemm_noalloc_debug_fail.argtypes = []
         L.lcgemm_strerror.argtypes = [i32]
         L.lcgemm_strerror.restype = ctypes.c_char_p
         for name in EXPORTS:

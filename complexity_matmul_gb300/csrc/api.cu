@@ -8,6 +8,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "kernels.h"
 #include "lcgemm.h"
@@ -61,6 +63,20 @@ bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, in
   const uint64_t strides[1] = {static_cast<uint64_t>(ld) * 2};
   const uint32_t box[2] = {64u, static_cast<uint32_t>(box_rows)};
   return encode_map(m, bf16, base, 2, dims, strides, box);
+}
+
+cudaError_t set_smem_limit(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;   // (kernel, device) pairs already opted in
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == kern && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(kern, dev);
+  return e;
 }
 
 }  // namespace lcg

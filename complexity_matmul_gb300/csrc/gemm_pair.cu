@@ -292,11 +292,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <bool BF16, bool EPI>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
   auto kern = plain_pair_kernel<BF16, EPI>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
 }

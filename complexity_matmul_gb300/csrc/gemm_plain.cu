@@ -125,8 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // The CTA is aborting: let every copy this thread started land first.
-        for (int s = 0; s < STAGES; ++s)
-          if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, wc, false);
+        drain_armed(full, STAGES, armed, armed_par, wc);
       }
     }
     __syncwarp();
@@ -352,11 +351,9 @@ template <int BN, int STAGES, bool BF16, bool EPI>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
   auto kern = plain_gemm_kernel<BN, STAGES, BF16, EPI>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_maybe_pdl(kern, L.grid, kThreads, C::kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
 }

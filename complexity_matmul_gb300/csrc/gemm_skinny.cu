@@ -246,8 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // The CTA is aborting: let every copy this thread started land first.
-        for (int s = 0; s < C::kStages; ++s)
-          if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, wc, false);
+        drain_armed(full, C::kStages, armed, armed_par, wc);
       }
     }
     __syncwarp();
@@ -384,11 +383,9 @@ cudaError_t launch_impl(const SkinnyLaunch& L, cudaStream_t stream) {
     return cudaErrorInvalidValue;   // the host never picks a stage that leaves no double buffering
   } else {
   auto kern = skinny_kernel<MP, SUB, BF16>;
-  static bool attr_set = false;   // per process; the attribute is per function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_maybe_pdl(kern, L.grid, kThreads, C::kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
   }

@@ -189,6 +189,16 @@ struct LcmaOperand {
   int r, c;
 };
 
+// Two-level Strassen, hierarchical: the 7 outer products each run as one
+// launch of the CTA-pair fused kernel over the inner (M/4 x N/4) block grid,
+// and every inner quadrant value it finishes goes to the outer level instead
+// of C: up to two targets per launch, each an FP32 outer slot (Init / Acc) or
+// C itself (Final: slot + sign * value, then the epilogue and the one cast).
+enum : int { kOuterNone = 0, kOuterInit = 1, kOuterAcc = 2, kOuterFinal = 3 };
+struct LcmaOuterTarget {
+  int kind, slot, sign, quad;     // quad: outer quadrant of C (2 * row + column)
+};
+
 struct LcmaArgs {
   void* C;
   int64_t ldc;
@@ -203,6 +213,11 @@ struct LcmaArgs {
   int debug_drop;                 // test hook: second halves never publish
   int raw2d;                      // CTA-pair path: raw-block maps are 2-D maps of the whole operand
   int group_order;                // CTA-pair path: 1 all pairs walk one product order; 0 odd pairs another
+  int outer;                      // CTA-pair path, two levels: inner quadrant values go to `otgt`
+  float* oslot;                   // outer FP32 slots: 3 x [2 * mbp / 128][2 * nbp][128] (128-row blocks,
+                                  // column-major inside: a warp's 32 rows of one column are one line)
+  int mbp, nbp;                   // inner block sizes rounded up to the 256 x 256 Group tile
+  LcmaOuterTarget otgt[2];
   int64_t ldp;
   int num_products;
   int* err;
@@ -219,6 +234,12 @@ struct LcmaLaunch {
   int grid;
   bool pdl;   // launch as a programmatic dependent of the preceding pre-pass kernel
 };
+
+// Opts kernel `kern` into `bytes` of dynamic shared memory on the current
+// device, once per (kernel, device).  The attribute belongs to each device's
+// copy of the function, so a process that drives several devices sets it on
+// each; callers on several host threads are serialised.
+cudaError_t set_smem_limit(const void* kern, int bytes);
 
 // Launches kern<<<grid, block, smem, st>>>(args...), as a programmatic dependent
 // of the previous kernel in `st` when `pdl` is set.

@@ -124,10 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, wc, false);
-      }
+      if (!ok) drain_armed(full, kStages, armed, armed_par, wc);   // aborting: let this thread's copies land
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -289,9 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok)
-        for (int s = 0; s < kStages; ++s)
-          if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, wc, false);
+      if (!ok) drain_armed(full, kStages, armed, armed_par, wc);   // aborting: let this thread's copies land
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -387,11 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool BF16>
 cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
   auto kern = lcma1_fused_kernel<BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw,
                           L.args);
@@ -405,12 +398,9 @@ cudaError_t launch_lcma_fused(const LcmaLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_lcma_products(const LcmaLaunch& L, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(lcma_products_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(lcma_products_kernel), kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_maybe_pdl(lcma_products_kernel, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum,
                           L.tmB_raw, L.args, L.bf16);

@@ -288,6 +288,47 @@ __device__ __forceinline__ void tile_coords_l2(int t, const LcmaArgs& a, int& mb
   nb = local / rows;
 }
 
+// Two levels: 32 FP32 values (one row, columns qcol .. qcol+31) of inner
+// quadrant `iq` of this launch's outer product P go to the outer level: into an
+// outer slot (Init / Acc), or, with the slot's sum, into outer quadrant q of C
+// (Final: epilogue, one cast).  Row rloc < mbp and column qcol < nbp always lie
+// inside the padded slots; only C's stores are bounded by its extents.
+template <bool BF16>
+__device__ __forceinline__ void apply_outer(const float (&v)[32], int iq, int rloc, int qcol, const LcmaArgs& a) {
+  const int ri = iq >> 1, ci = iq & 1;
+  const int pr = ri * a.mbp + rloc;                      // row of P (and of every outer slot)
+  const int pc = ci * a.nbp + qcol;
+  const int64_t slot_floats = static_cast<int64_t>(2 * a.mbp) * (2 * a.nbp);
+  const int64_t off = (static_cast<int64_t>(pr >> 7) * (2 * a.nbp) + pc) * 128 + (pr & 127);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const LcmaOuterTarget t = a.otgt[i];
+    if (t.kind == kOuterNone) continue;
+    float* sp = a.oslot + t.slot * slot_floats + off;
+    const float sg = static_cast<float>(t.sign);
+    if (t.kind == kOuterInit) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sp[j * 128] = sg * v[j];
+    } else if (t.kind == kOuterAcc) {
+      float w[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = sp[j * 128];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sp[j * 128] = w[j] + sg * v[j];
+    } else {
+      float w[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = sp[j * 128] + sg * v[j];
+      const int qr = t.quad >> 1, qc = t.quad & 1;
+      const int64_t row = static_cast<int64_t>(qr) * 2 * a.mb + static_cast<int64_t>(ri) * a.mb + rloc;
+      const int64_t col = static_cast<int64_t>(qc) * 2 * a.nb + static_cast<int64_t>(ci) * a.nb + qcol;
+      if (rloc < a.mb && qcol < a.nb && row < a.M && col < a.N)
+        store_run<BF16, 32>(static_cast<uint16_t*>(a.C) + row * a.ldc + col, row, col,
+                            min(min(32, a.nb - qcol), static_cast<int>(a.N - col)), w, a.ep);
+    }
+  }
+}
+
 // Consume one product held in TMEM (this thread: one row, 128 columns) into
 // the scratch slots / C according to the step's targets.
 // `col0`: first of this thread's 128 columns inside the tile; `tile_col0`: the
@@ -335,15 +376,19 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += __ldcg(pp + j * kRows);
         }
-        // epilogue, cast once and store into quadrant t.quad of C
-        const int qr = t.quad >> 1, qc = t.quad & 1;
-        const int64_t crow_i = static_cast<int64_t>(qr) * a.mb + rloc;
-        uint16_t* crow = Cp + crow_i * a.ldc + static_cast<int64_t>(qc) * a.nb;
         const int qcol = tile_col0 + col;              // column inside the quadrant
-        const int64_t gcol = static_cast<int64_t>(qc) * a.nb + qcol;
-        if (rloc < a.mb && qcol < a.nb && crow_i < a.M && gcol < a.N)
-          store_run<BF16, 32>(crow + qcol, crow_i, gcol, min(min(32, a.nb - qcol), static_cast<int>(a.N - gcol)), v,
-                              a.ep);
+        if (a.outer) {
+          apply_outer<BF16>(v, t.quad, rloc, qcol, a);
+        } else {
+          // epilogue, cast once and store into quadrant t.quad of C
+          const int qr = t.quad >> 1, qc = t.quad & 1;
+          const int64_t crow_i = static_cast<int64_t>(qr) * a.mb + rloc;
+          uint16_t* crow = Cp + crow_i * a.ldc + static_cast<int64_t>(qc) * a.nb;
+          const int64_t gcol = static_cast<int64_t>(qc) * a.nb + qcol;
+          if (rloc < a.mb && qcol < a.nb && crow_i < a.M && gcol < a.N)
+            store_run<BF16, 32>(crow + qcol, crow_i, gcol, min(min(32, a.nb - qcol), static_cast<int>(a.N - gcol)),
+                                v, a.ep);
+        }
       }
     }
   }
@@ -495,6 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs, 8 warps)
+    if (args_in.outer) griddep_wait();   // the outer slots come from the launch before this one
     const int ew = warp - 2;
     const int q = warp & 3;                 // TMEM lane quarter
     const int half = ew >> 2;               // which 128 of the 256 columns
@@ -555,11 +601,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <bool BF16>
 cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
   auto kern = lcma1_l2_kernel<BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw,
                           L.args);
@@ -570,7 +614,8 @@ cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
 size_t lcma_pair_scratch_bytes(int grid) { return static_cast<size_t>(grid) * kSlots * kSlotFloats * sizeof(float); }
 
 cudaError_t launch_lcma_pair(const LcmaLaunch& L, cudaStream_t st) {
-  if (L.levels != 1 || L.grid % 2 || !L.args.scratch) return cudaErrorInvalidValue;
+  if (L.levels != (L.args.outer ? 2 : 1) || L.grid % 2 || !L.args.scratch) return cudaErrorInvalidValue;
+  if (L.args.outer && !L.args.oslot) return cudaErrorInvalidValue;
   return L.bf16 ? launch_impl<true>(L, st) : launch_impl<false>(L, st);
 }
 

@@ -46,6 +46,55 @@ int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st) {
 
 namespace {
 
+// Outer level of hierarchical two-level Strassen: the order of the 7 outer
+// products (one launch each) and where each launch's product P goes, over
+// three FP32 outer slots of M/2 x N/2.  The order M5 M3 M7 M1 M4 M2 M6 keeps
+// at most three outer quadrants live (C12 retires after M3, C11 after M4,
+// C21 after M2, C22 after M6).
+struct OuterStep {
+  int product;
+  LcmaOuterTarget t[2];
+};
+constexpr OuterStep kOuterProgram[7] = {
+    {4, {{kOuterInit, 0, -1, 0}, {kOuterInit, 1, 1, 1}}},    // M5: s0 = -P (C11), s1 = P (C12)
+    {2, {{kOuterFinal, 1, 1, 1}, {kOuterInit, 1, 1, 3}}},   // M3: C12 = s1 + P; s1 = P (C22)
+    {6, {{kOuterAcc, 0, 1, 0}, {kOuterNone, 0, 0, 0}}},     // M7: s0 += P
+    {0, {{kOuterAcc, 0, 1, 0}, {kOuterAcc, 1, 1, 3}}},      // M1: s0 += P, s1 += P
+    {3, {{kOuterFinal, 0, 1, 0}, {kOuterInit, 2, 1, 2}}},   // M4: C11 = s0 + P; s2 = P (C21)
+    {1, {{kOuterFinal, 2, 1, 2}, {kOuterAcc, 1, -1, 3}}},   // M2: C21 = s2 + P; s1 -= P
+    {5, {{kOuterFinal, 1, 1, 3}, {kOuterNone, 0, 0, 0}}},   // M6: C22 = s1 + P
+};
+
+// Symbolic run: every outer quadrant is stored once and equals sum_p W[q,p] P_p;
+// within a step, a target that reads a slot comes before one that rewrites it.
+constexpr bool outer_program_ok() {
+  int slot[3][7] = {};
+  bool written[3] = {};
+  bool done[4] = {};
+  for (const OuterStep& st : kOuterProgram) {
+    for (int i = 0; i < 2; ++i) {
+      const LcmaOuterTarget t = st.t[i];
+      if (t.kind == kOuterNone) continue;
+      if (t.kind != kOuterInit && !written[t.slot]) return false;
+      if (t.kind == kOuterInit) {
+        for (int j = 0; j < 7; ++j) slot[t.slot][j] = 0;
+        slot[t.slot][st.product] = t.sign;
+        written[t.slot] = true;
+      } else if (t.kind == kOuterAcc) {
+        slot[t.slot][st.product] += t.sign;
+      } else {
+        if (done[t.quad]) return false;
+        done[t.quad] = true;
+        for (int j = 0; j < 7; ++j)
+          if (slot[t.slot][j] + (j == st.product ? t.sign : 0) != kW1[t.quad][j]) return false;
+      }
+    }
+    if (st.t[0].kind == kOuterInit && st.t[1].kind >= kOuterAcc && st.t[0].slot == st.t[1].slot) return false;
+  }
+  return done[0] && done[1] && done[2] && done[3];
+}
+static_assert(outer_program_ok(), "the outer program must compute C_q = sum_p W[q,p] P_p");
+
 // M, N, K: the (divisible) operand extents; Mc x Nc: C's extents (smaller when the
 // operands are zero-padded copies).
 template <int L>
@@ -58,16 +107,26 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   const int na = plan.side[0].nslots, nbs = plan.side[1].nslots;
   const int64_t a_bytes = round_up(na * mb * kb * 2, 256);
   const int64_t b_bytes = round_up(nbs * nb * kb * 2, 256);
+  // fused Groups run on CTA pairs (256 x 256 tiles) unless the block is small; one level
+  // also has the single-CTA fused kernel, two levels otherwise run unfused
+  const bool pair = fused && grid_cap(h) >= 2 && (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
+  if (L == 2 && !pair) fused = false;
+  const bool hier = L == 2 && pair;           // seven launches, one per outer product
+  const int64_t mbp = round_up(mb, 256), nbp = round_up(nb, 256);
   const int64_t ldp = round_up(nb, 4);
   const int64_t p_bytes = fused ? 0 : round_up(int64_t(plan.R) * mb * ldp * 4, 256);
   const int64_t s_bytes = fused ? round_up(static_cast<int64_t>(lcma_pair_scratch_bytes(grid_cap(h))), 256) : 0;
-  const int64_t f_bytes = fused ? round_up(int64_t(sizeof(int)) * grid_cap(h), 256) : 0;   // split flags
-  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes + s_bytes + f_bytes), st);
+  const int launches = hier ? 7 : 1;
+  const int64_t f_bytes = fused ? round_up(int64_t(sizeof(int)) * grid_cap(h) * launches, 256) : 0;   // split flags
+  const int64_t o_bytes = hier ? 3 * (2 * mbp) * (2 * nbp) * 4 : 0;                                // outer slots
+  int rc = ensure_workspace(h, static_cast<size_t>(a_bytes + b_bytes + p_bytes + s_bytes + f_bytes + o_bytes), st);
   if (rc) return rc;
   uint16_t* wsA = static_cast<uint16_t*>(h->ws);
   uint16_t* wsB = reinterpret_cast<uint16_t*>(static_cast<char*>(h->ws) + a_bytes);
   float* prod = reinterpret_cast<float*>(static_cast<char*>(h->ws) + a_bytes + b_bytes);
   float* scratch = reinterpret_cast<float*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes);
+  float* oslot =
+      reinterpret_cast<float*>(static_cast<char*>(h->ws) + a_bytes + b_bytes + p_bytes + s_bytes + f_bytes);
 
   // ---- Combine-A/B pre-pass
   CombineArgs ca{};
@@ -81,9 +140,6 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
   if (launch_combine_ab(ca, L, bf16, h->num_sms, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
 
   // ---- products
-  // fused one-level Groups run on CTA pairs (256 x 256 tiles) unless the quadrant is small
-  const bool pair = fused && L == 1 && grid_cap(h) >= 2 &&
-                    (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
   const int b_box = 128;
   LcmaLaunch ll{};
   ll.levels = L;
@@ -159,7 +215,34 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
     a.raw2d = raw2d ? 1 : 0;
     a.group_order = h->group_order;
     ll.grid = 2 * std::min(a.num_items, P);
-    if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    if (!hier) {
+      if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+      return LCGEMM_OK;
+    }
+    // two levels: outer product po runs the one-level kernel on the inner products
+    // p = 7 * po + pi of the two-level tables; its four inner quadrants go to the
+    // outer targets (stream order, and each launch's wait for the one before it,
+    // keep the outer slots consistent)
+    LcmaOperand as[49], bs[49];
+    for (int p = 0; p < plan.R; ++p) {
+      as[p] = a.a_src[p];
+      bs[p] = a.b_src[p];
+    }
+    a.outer = 1;
+    a.oslot = oslot;
+    a.mbp = static_cast<int>(mbp);
+    a.nbp = static_cast<int>(nbp);
+    for (int step = 0; step < 7; ++step) {
+      const OuterStep& os = kOuterProgram[step];
+      for (int pi = 0; pi < 7; ++pi) {
+        a.a_src[pi] = as[7 * os.product + pi];
+        a.b_src[pi] = bs[7 * os.product + pi];
+      }
+      a.otgt[0] = os.t[0];
+      a.otgt[1] = os.t[1];
+      a.flags = split ? flags + step * grid_cap(h) : nullptr;
+      if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+    }
     return LCGEMM_OK;
   }
   if (fused) {

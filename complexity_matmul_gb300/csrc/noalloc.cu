@@ -16,7 +16,9 @@
 //   * every call on a device uses the same array, so calls that overlap on the
 //     GPU (different streams, or other host threads) race; serialise them;
 //   * the array keeps the previous call's contents; the only value that must
-//     start at zero (the device error word) is cleared on every call;
+//     start at zero, the device error word, is zero when the library is
+//     loaded and is cleared again only by lcgemm_noalloc_status, so an error
+//     stays visible until the caller asks for it;
 //   * the first call on each device looks up the array's device address with
 //     cudaGetSymbolAddress (with that device current) and caches it.
 #include <algorithm>
@@ -26,6 +28,7 @@
 #include "kernels.h"
 #include "lcgemm.h"
 #include "lcma_tables.h"
+#include "ptx.cuh"
 #include "runtime.h"
 
 namespace {
@@ -82,16 +85,25 @@ extern "C" LCGEMM_API int lcgemm_strassen1_noalloc(int64_t M, int64_t N, int64_t
   if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return LCGEMM_ERR_ARG;
   if (dtype != LCGEMM_F16 && dtype != LCGEMM_BF16) return LCGEMM_ERR_ARG;
   if (M == 0 || N == 0) return LCGEMM_OK;
-  if (!A || !B || !C || lda < K || ldb < K || ldc < N) return LCGEMM_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15u)
+  // with K = 0 A and B are not read (and may be null), as for lcgemm_run
+  if (!C || ldc < N || (K > 0 && (!A || !B || lda < K || ldb < K))) return LCGEMM_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) & 15u) || (ldc & 7)) return LCGEMM_ERR_ALIGN;
+  if (K > 0 && (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) || ((lda | ldb) & 7)))
     return LCGEMM_ERR_ALIGN;
-  if ((lda | ldb | ldc) & 7) return LCGEMM_ERR_ALIGN;
-  if (M % 2 || N % 2 || K % 16 || K == 0) return LCGEMM_ERR_UNSUPPORTED;
-  {
+  if (M % 2 || N % 2 || K % 16) return LCGEMM_ERR_UNSUPPORTED;
+  if (K > 0) {
     const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), c1 = c0 + uintptr_t((M - 1) * ldc + N) * 2;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(A), a1 = a0 + uintptr_t((M - 1) * lda + K) * 2;
     const uintptr_t b0 = reinterpret_cast<uintptr_t>(B), b1 = b0 + uintptr_t((N - 1) * ldb + K) * 2;
     if ((c0 < a1 && a0 < c1) || (c0 < b1 && b0 < c1)) return LCGEMM_ERR_ALIAS;
+  }
+
+  if (K == 0) {
+    // an empty product: C = 0, as lcgemm_run gives (a 2-D memset allocates nothing)
+    return cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(N) * 2, static_cast<size_t>(M),
+                             static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+               ? LCGEMM_OK
+               : LCGEMM_ERR_CUDA;
   }
 
   constexpr LcmaPlan<1> plan{};
@@ -112,7 +124,6 @@ extern "C" LCGEMM_API int lcgemm_strassen1_noalloc(int64_t M, int64_t N, int64_t
   uint16_t* wsB = reinterpret_cast<uint16_t*>(scratch + kErrBytes + a_bytes);
   const bool bf16 = dtype == LCGEMM_BF16;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return LCGEMM_ERR_CUDA;
 
   CombineArgs ca{};
   ca.side[0] = CombineSide{static_cast<const uint16_t*>(A), lda, wsA, kb, mb * kb, mb, kb, mb * kb / 8};
@@ -160,5 +171,35 @@ extern "C" LCGEMM_API int lcgemm_strassen1_noalloc(int64_t M, int64_t N, int64_t
   a.timeout_ns = 2000000000ull;
   ll.grid = std::min(a.num_groups, num_sms);
   if (launch_lcma_fused(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+  return LCGEMM_OK;
+}
+
+// The error word is the first int of the array; both calls work on the current
+// device's copy with synchronous symbol copies into and out of a host integer.
+extern "C" LCGEMM_API int lcgemm_noalloc_status(void* cuda_stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return LCGEMM_ERR_CUDA;
+  }
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_noalloc_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return LCGEMM_ERR_CUDA;
+  }
+  if (word == 0) return LCGEMM_OK;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(int), 0, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return LCGEMM_ERR_CUDA;
+  }
+  return LCGEMM_ERR_TIMEOUT;
+}
+
+extern "C" LCGEMM_API int lcgemm_noalloc_debug_fail(void) {
+  const int word = kErrWaitTimeout;
+  if (cudaMemcpyToSymbol(g_noalloc_scratch, &word, sizeof(int), 0, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return LCGEMM_ERR_CUDA;
+  }
   return LCGEMM_OK;
 }

@@ -356,6 +356,18 @@ __device__ __forceinline__ uint32_t ld_acquire_cluster_u32(uint32_t addr_cluster
   return v;
 }
 
+// Abort path of a TMA producer: waits for the copies this thread started on the
+// armed stages (`armed`: bit per stage, `armed_par`: the phase parity each was
+// armed in) so that none lands after the CTA has left; the wait is bounded but
+// lasts at least 1 ms however short the configured limit is.
+__device__ __forceinline__ void drain_armed(uint64_t* full, int stages, uint32_t armed, uint32_t armed_par,
+                                            const WaitCtl& wc) {
+  WaitCtl w = wc;
+  if (w.timeout_ns < 1000000ull) w.timeout_ns = 1000000ull;
+  for (int s = 0; s < stages; ++s)
+    if (armed >> s & 1u) mbar_wait(&full[s], (armed_par >> s) & 1u, w, false);
+}
+
 // Bounded spin used only on the abort path: gives copies already in flight
 // time to land before the CTA leaves.
 __device__ __forceinline__ void settle_ns(uint64_t ns) {

@@ -42,8 +42,15 @@ namespace {
 // bandwidth the streaming kernels reach.  Measured on GB300 (1 CTA per SM).
 constexpr double kEtaPlainPair = 0.86;    // CTA-pair 256 x 256 tiles
 constexpr double kEtaPlainSingle = 0.78;  // single-CTA 128 x 256 tiles
-constexpr double kEtaLcmaPair = 0.70;     // fused one-level Groups on CTA pairs (256 x 256, 7 products)
 constexpr double kEtaLcmaSingle = 0.55;   // single-CTA 128 x 128 product tiles (shared-memory bound)
+// Fused one-level Groups on CTA pairs (256 x 256, 7 products): each product
+// streams the same operand bytes per flop as a plain CTA-pair tile, but every
+// switch to the next product's operand panels costs about this many 64-deep K
+// slabs of MMA time (pipeline refill from L2 misses), so the products run at
+// kEtaPlainPair * (1 - kLcmaSwitchSlabs / slabs per product).  Measured on
+// GB300 against the plain kernel in the same process: 0.76 of its rate at 32
+// slabs per product, 0.87-0.89 at 64, 0.93 at 128.
+constexpr double kLcmaSwitchSlabs = 8.0;
 constexpr double kBetaStream = 0.80;      // combine pre-pass / recombination, fraction of HBM bandwidth
 constexpr double kLaunchSec = 6e-6;       // launch + prologue + pipeline fill of one kernel
 
@@ -144,7 +151,9 @@ double estimate_divisible(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, i
       if (pair) {
         const int64_t groups = cdiv(mb, 256) * cdiv(nb, 256);
         const double eff = h->split ? wave_efficiency_split(groups, sms / 2) : wave_efficiency(groups, sms / 2);
-        const double t = std::max(flops / (kEtaLcmaPair * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
+        const double slabs = static_cast<double>(cdiv(K / 2, 64));
+        const double eta = kEtaPlainPair * std::max(0.1, 1.0 - kLcmaSwitchSlabs / slabs);
+        const double t = std::max(flops / (eta * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
         return t_pre + t;
       }
       return t_pre + kernel_time(flops, bytes, cdiv(mb, 128) * cdiv(nb, 128), sms, kEtaLcmaSingle, P, BW);
@@ -158,6 +167,19 @@ double estimate_divisible(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, i
     const int64_t mb = M / 4, nb = N / 4;
     const double t_pre = kernel_time(0, 7.625 * (m * k + k * n), 0, 1, 1.0, P, BW);
     const double flops = 49.0 / 64.0 * mnk2;
+    const bool pair = sms >= 2 && (h->lcma_kernel == 2 || (h->lcma_kernel == 0 && mb > 128));
+    if (pair) {
+      // hierarchical: seven launches of the one-level CTA-pair kernel over the inner
+      // (M/4 x N/4) grid; the outer level goes through three FP32 slots of M/2 x N/2
+      // (eight slot writes and eight reads of MN bytes each, then C)
+      const int64_t groups = cdiv(mb, 256) * cdiv(nb, 256);
+      const double eff = h->split ? wave_efficiency_split(groups, sms / 2) : wave_efficiency(groups, sms / 2);
+      const double slabs = static_cast<double>(cdiv(K / 4, 64));
+      const double eta = kEtaPlainPair * std::max(0.1, 1.0 - kLcmaSwitchSlabs / slabs);
+      const double bytes = (6.125 * (m * k + k * n) + 16.0 * m * n + 2.0 * m * n) / 7.0;   // per launch
+      const double t = std::max(flops / 7.0 / (eta * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
+      return t_pre + 7.0 * t;
+    }
     // unfused: 49 FP32 products of (M/4 x N/4) written and read back, then C
     const double t_prod = kernel_time(flops, 6.125 * (m * k + k * n) + 12.25 * m * n,
                                       49 * cdiv(mb, 128) * cdiv(nb, 128), sms, kEtaLcmaSingle, P, BW);
@@ -193,7 +215,7 @@ int dispatch(lcgemm_ctx* h, int algo, int64_t M, int64_t N, int64_t K, const voi
     case LCGEMM_STRASSEN1_UNFUSED:
       return run_strassen(h, 1, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
     case LCGEMM_STRASSEN2:
-      return run_strassen(h, 2, false, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
+      return run_strassen(h, 2, true, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
     default:
       return LCGEMM_ERR_UNSUPPORTED;
   }

@@ -119,7 +119,7 @@ enum {
                                       stream-K skinny kernel (M <= 256), 4 the CUDA-core GEMV
                                       (M <= 4); for 3 and 4 larger M choose                            */
   LCGEMM_OPT_LCMA_KERNEL = 9,       /* fused one-level Strassen kernel: 0 choose (default), 1
-                                      single-CTA 128x128 Groups, 2 CTA-pair 256x128 Groups           */
+                                      single-CTA 128x128 Groups, 2 CTA-pair 256x256 Groups           */
   LCGEMM_OPT_PDL = 10               /* 1 (default): launch the GEMM kernels (plain tiles, GEMV,
                                       skinny, Strassen products) as programmatic dependents of the
                                       kernel before them: their prologue (barriers, tensor memory,
@@ -255,20 +255,40 @@ LCGEMM_API int lcgemm_set_option(lcgemm_t h, int option, int64_t value);
  * exits, and the call makes no cudaMalloc, cudaFree or other allocating call.
  *
  * Arguments, layouts and alignment rules are those of lcgemm_run; requires M,
- * N even and K a multiple of 16 (else LCGEMM_ERR_UNSUPPORTED).  The summed
- * operands take 2.5 * K * (M + N) bytes plus alignment; larger problems fail
- * with LCGEMM_ERR_TOO_LARGE (e.g. M = N = K = 1792 fits, 2048 does not).
+ * N even and K a multiple of 16 (else LCGEMM_ERR_UNSUPPORTED); K = 0 fills C
+ * with zeros (no kernel but a 2-D memset; A and B are then not read and may be
+ * NULL).  The summed operands take
+ * 2.5 * K * (M + N) bytes plus alignment; larger problems fail with
+ * LCGEMM_ERR_TOO_LARGE (e.g. M = N = K = 1792 fits, 2048 does not).
  * Runs asynchronously on `cuda_stream`.  All calls on a device share the one
  * array: calls that overlap on the GPU (other streams, other threads) race and
- * must be serialised by the caller.  The array keeps the previous call's data;
- * its error word is cleared on every call.  Bounded device-side waits still
- * end the kernel if they run out, but this entry point does not report them.
- * The first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture.
+ * must be serialised by the caller.  The array keeps the previous call's data.
+ * A bounded device-side wait that runs out ends the kernel early (C is then
+ * partly written) and sets the array's error word, which stays set until
+ * lcgemm_noalloc_status reads and clears it.  The first call on each device
+ * looks up the array's device address (with that device current); make that
+ * first call before any stream capture.
  */
 LCGEMM_API int lcgemm_strassen1_noalloc(int64_t M, int64_t N, int64_t K,
                                         const void* A, int64_t lda, const void* B, int64_t ldb,
                                         void* C, int64_t ldc, int dtype, void* cuda_stream);
+
+/*
+ * Status of lcgemm_strassen1_noalloc on the current device, without
+ * allocating: synchronises `cuda_stream`, reads the fixed array's error word
+ * with a synchronous copy into a host integer, clears it, and returns
+ * LCGEMM_ERR_TIMEOUT if any call since the last query had a device-side wait
+ * run out (LCGEMM_OK otherwise; LCGEMM_ERR_CUDA if the synchronisation or the
+ * copy fails).  The paper has no counterpart to this entry point.
+ */
+LCGEMM_API int lcgemm_noalloc_status(void* cuda_stream);
+
+/*
+ * Test hook: sets the error word of lcgemm_strassen1_noalloc on the current
+ * device as a wait that ran out would (synchronous, allocates nothing), so a
+ * caller's error handling can be exercised without a device-side failure.
+ */
+LCGEMM_API int lcgemm_noalloc_debug_fail(void);
 
 /* Static description of a status code (never NULL). */
 LCGEMM_API const char* lcgemm_strerror(int code);

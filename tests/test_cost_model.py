@@ -148,3 +148,59 @@ def test_degenerate_shapes(plan):
     assert est(-1, 128, 128)[0] == lcg.ERR_ARG
     assert est(128, 128, 128, dtype=7)[0] == lcg.ERR_ARG
     assert est(128, 128, 128, algo=9)[0] == lcg.ERR_ARG
+
+
+def _h20_like():
+    """A bandwidth-rich, compute-poor part like the write-up's H20 (about 148 TFLOP/s dense FP16,
+    4 TB/s HBM, 78 SMs): FalconGEMM write-up, section "从 LCMA 到 FalconGEMM" (H20 suits trading
+    extra data handling for fewer multiplications) and "从缓存重排到 Cost Model" (LCMA only pays
+    where the GEMM is compute-bound)."""
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    h.set_option(lcg.OPT_PEAK_GFLOPS, 148_000)
+    h.set_option(lcg.OPT_HBM_GBPS, 4_000)
+    h.set_option(lcg.OPT_MAX_CTAS, 78)
+    return h
+
+
+def test_h20_like_machine_picks_strassen_only_for_large_cubes():
+    """On a machine with ~15x less tensor throughput per byte of bandwidth the model must pick
+    Strassen for large compute-bound cubes and keep plain for the shapes where the
+    pre-pass or the per-product pipeline refills outweigh the 1/8 of multiplications saved.
+    A Strassen efficiency that cannot reach 7/8 of plain's never picks it (first assertion);
+    a model without the refill cost picks it at 8192^3 too (second)."""
+    h = _h20_like()
+    for n in (12288, 16384):
+        assert h.select(n, n, n, lcg.BF16) in (lcg.STRASSEN1, lcg.STRASSEN2), n
+    # a second level pays once the cube is large enough to amortise its larger pre-pass
+    assert h.select(24576, 24576, 24576, lcg.BF16) == lcg.STRASSEN2
+    for n in (2048, 4096, 8192):
+        assert h.select(n, n, n, lcg.BF16) == lcg.PLAIN, n
+    h.close()
+
+
+def test_gb300_model_keeps_plain_on_the_measured_shapes(plan):
+    """On GB300 the plain CTA-pair kernel was the fastest algorithm on every shape measured (the
+    square sweep, the large rectangles, all 1000 grid shapes): the model must not pick Strassen
+    there.  A model that drops the per-product refill cost picks strassen1 at 16384^3."""
+    import synthetic
+    for n in (2048, 4096, 8192, 16384):
+        assert plan.select(n, n, n, lcg.BF16) == lcg.PLAIN, n
+    for shape in synthetic.LARGE_RECT:
+        assert plan.select(*shape, lcg.BF16) == lcg.PLAIN, shape
+    picks = [plan.select(M, N, K, lcg.F16) for (M, N, K) in synthetic.grid_triples()]
+    assert picks.count(lcg.PLAIN) == len(picks)
+
+
+def test_prepass_is_priced_at_streaming_bandwidth(plan):
+    """The Combine-A/B pre-pass reads A and B once and writes five summed blocks of each (the
+    other two products read raw blocks in place): 4.5 bytes per element of A and B, priced at the
+    model's streaming fraction (0.8) of the HBM bandwidth.  Removing the bandwidth (1e9 GB/s)
+    removes exactly that time from a compute-bound one-level estimate."""
+    h = lcg.Handle(lcg.PLANNING_DEVICE)
+    M, N, K = 16384, 16384, 16384
+    t_bw = h.estimate(M, N, K, lcg.BF16, "strassen1")
+    h.set_option(lcg.OPT_HBM_GBPS, 1_000_000_000)
+    t_inf = h.estimate(M, N, K, lcg.BF16, "strassen1")
+    h.close()
+    expect = 4.5 * (M * K + K * N) / (0.8 * 8000e9)
+    assert abs((t_bw - t_inf) - expect) < 0.02 * expect
