@@ -194,6 +194,18 @@ int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K) {
   return (M > 128 && N > 128 && pair_tiles >= grid_cap(h) / 4) ? 2 : 1;
 }
 
+// Tile width of the single-CTA kernel: 256 columns, 128 for narrow C, and 96
+// when C has one tile row whose 96-column tiles about fill the SMs (N = 14336
+// on 152 SMs: 150 tiles), so that every SM streams its own slice of B once and
+// no split-K hand-off is needed.
+int plain_single_bn(int64_t M, int64_t N, int sms) {
+  if (M <= kPlainBM) {
+    const int64_t t96 = (N + 95) / 96;
+    if (t96 <= sms && t96 * 100 >= int64_t(85) * sms) return 96;
+  }
+  return N <= 128 ? 128 : 256;
+}
+
 int run_gemv(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
              int64_t ldc, bool bf16, const Epilogue& ep, bool pdl, cudaStream_t st) {
   GemvArgs a{};
@@ -289,7 +301,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   L.pdl = h->pdl != 0;
   const bool pair = variant == 2;
   const int bm = pair ? 2 * kPlainBM : kPlainBM;
-  L.bn = pair ? 256 : (N <= 128 ? 128 : 256);
+  L.bn = pair ? 256 : plain_single_bn(M, N, grid_cap(h));
   if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, kPlainBM)) return LCGEMM_ERR_CUDA;
   if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, pair ? L.bn / 2 : L.bn)) return LCGEMM_ERR_CUDA;
   PlainArgs& a = L.args;

@@ -36,10 +36,11 @@ struct Cfg {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kAccCols = BN <= 128 ? 128 : 256;       // accumulator stride (128-column aligned)
+  static constexpr int kTmemCols = 2 * kAccCols;                // two accumulators, a power of two
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
-  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
+  static_assert(2 * BN <= kTmemCols && BN % 32 == 0, "accumulator columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, wc)) {
             ok = false;
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
       if (args.splits == 1) {
         if constexpr (EPI) {
           // the next chunk's bias / residual loads are in flight while this chunk is finished
@@ -370,6 +371,8 @@ cudaError_t launch_reduce_impl(const PlainLaunch& L, cudaStream_t stream) {
 cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream) {
   if (L.bn == 256) return L.bf16 ? launch_reduce_impl<256, true>(L, stream)
                                  : launch_reduce_impl<256, false>(L, stream);
+  if (L.bn == 96) return L.bf16 ? launch_reduce_impl<96, true>(L, stream)
+                                : launch_reduce_impl<96, false>(L, stream);
   if (L.bn == 128) return L.bf16 ? launch_reduce_impl<128, true>(L, stream)
                                  : launch_reduce_impl<128, false>(L, stream);
   return cudaErrorInvalidValue;
@@ -380,9 +383,11 @@ cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream) {
   if (L.args.ep.on) {
     if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true, true>(L, stream) : launch_impl<256, 4, false, true>(L, stream);
     if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true, true>(L, stream) : launch_impl<128, 6, false, true>(L, stream);
+    if (L.bn == 96) return L.bf16 ? launch_impl<96, 7, true, true>(L, stream) : launch_impl<96, 7, false, true>(L, stream);
   }
   if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true, false>(L, stream) : launch_impl<256, 4, false, false>(L, stream);
   if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true, false>(L, stream) : launch_impl<128, 6, false, false>(L, stream);
+  if (L.bn == 96) return L.bf16 ? launch_impl<96, 7, true, false>(L, stream) : launch_impl<96, 7, false, false>(L, stream);
   return cudaErrorInvalidValue;
 }
 

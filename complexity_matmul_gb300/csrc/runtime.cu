@@ -107,7 +107,7 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
     }
     // single-CTA tiles with the launcher's split-K: tiles x chunks work items, FP32
     // partials written and read back, deep splits summed by a separate kernel
-    const int64_t bn = N <= 128 ? 128 : 256;
+    const int64_t bn = plain_single_bn(M, N, sms);
     const int64_t tiles = cdiv(M, 128) * cdiv(N, bn), num_kb = cdiv(K, 64);
     int64_t splits = 1;
     if (tiles < sms / 2 && num_kb >= kSplitKMinSlabs) splits = std::max<int64_t>(1, std::min<int64_t>(sms / tiles, num_kb / 16));

@@ -44,6 +44,7 @@ bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uin
                 const uint64_t* strides_bytes, const uint32_t* box);
 bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows);
 int grid_cap(const lcgemm_ctx* h);
+int plain_single_bn(int64_t M, int64_t N, int sms);
 int ensure_workspace(lcgemm_ctx* h, size_t bytes, cudaStream_t st);
 // True while `st` is capturing a CUDA graph (no allocation or synchronisation allowed then).
 bool capturing(cudaStream_t st);

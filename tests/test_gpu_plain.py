@@ -7,7 +7,7 @@ import torch
 
 import complexity_matmul_gb300 as lcg
 import synthetic
-from helpers import assert_bit_exact, assert_close, oracle_c64
+from helpers import assert_bit_exact, assert_close, oracle_c64, oracle_epilogue, padded
 
 pytestmark = pytest.mark.gpu
 
@@ -252,3 +252,28 @@ def test_fp16_grid_shapes_sampled_rows(h, M, N, K):
     assert h.sync_status() == 0
     rows = synthetic.row_sample(M, 64)
     assert_close(C, oracle_c64(A, B, "f16", rows=rows), "f16", "plain", rows=rows)
+
+
+# ---------------------------------------------------------------- one tile row on 96-column tiles
+
+@pytest.mark.parametrize("M,N,K", [(16, 14336, 4096), (128, 14336, 4096), (3, 14300, 4104), (100, 13000, 520)])
+def test_one_row_96_column_tiles(M, N, K):
+    """C with one 128-row tile row whose 96-column tiles about fill the SMs (150 tiles for N = 14336)
+    runs on the single-CTA kernel with BN = 96 and no split-K: integer inputs bit-exact, ragged N and
+    K included; and the fused epilogue on the same tiles."""
+    h = lcg.Handle(0)
+    A, B = synthetic.operands(M, N, K, "int3", 71, "bf16", "cuda")
+    Ap, Bp = padded(M, K, "bf16", A), padded(N, K, "bf16", B)
+    C = h.run(Ap, Bp, algo="plain")
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
+    if M == 100:
+        b = synthetic.matrix(1, N, "int3", 72, "bf16", "cuda")[0]
+        R = padded(M, N, "bf16", synthetic.matrix(M, N, "int3", 73, "bf16", "cuda"))
+        D64, _ = oracle_epilogue(A, B, "bf16", b, R, "relu")
+        C = h.run(Ap, Bp, algo="plain", bias=b, residual=R, act="relu")
+        torch.cuda.synchronize()
+        assert h.sync_status() == 0
+        assert_bit_exact(C, D64, "bf16")
+    h.close()
