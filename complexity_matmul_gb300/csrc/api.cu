@@ -302,7 +302,9 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   const bool pair = variant == 2;
   const int bm = pair ? 2 * kPlainBM : kPlainBM;
   L.bn = pair ? 256 : plain_single_bn(M, N, grid_cap(h));
-  if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, kPlainBM)) return LCGEMM_ERR_CUDA;
+  // one tile row: the A box covers only the rows that exist (a multiple of 8)
+  const int a_rows = (!pair && M < kPlainBM) ? static_cast<int>((M + 7) / 8 * 8) : kPlainBM;
+  if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, a_rows)) return LCGEMM_ERR_CUDA;
   if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, pair ? L.bn / 2 : L.bn)) return LCGEMM_ERR_CUDA;
   PlainArgs& a = L.args;
   a.C = C;
@@ -323,6 +325,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   a.kb_per_split = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
   // one tile row: each B tile is read by one CTA (per K chunk) and never again
   a.b_read_once = (!pair && a.tiles_m == 1) ? 1 : 0;
+  a.a_rows = a_rows;
   if (!pair) {
     // Too few tiles to fill the machine (skinny M, small N) and a long enough K
     // (kSplitKMinSlabs): cut K into chunks of at least 16 slabs so that

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(args.a_rows * kBK * 2 + C::kBBytes));
           tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * kBK, mb * kBM);
           if (args.b_read_once)
             tma_load_2d_hint(sB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, nb * BN, b_policy);

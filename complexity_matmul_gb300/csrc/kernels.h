@@ -53,6 +53,11 @@ struct PlainArgs {
   // single-CTA kernel: every B tile is read once (one tile row): its loads
   // carry an L2 evict-first policy
   int b_read_once;
+  // single-CTA kernel: rows per A box (a multiple of 8, at most 128).  With one
+  // tile row only the rows that exist are copied; the MMA's rows past them read
+  // whatever the stage held before, into accumulator rows that are never stored
+  // or published, so each stage moves A bytes for M rows instead of 128.
+  int a_rows;
 };
 
 struct PlainLaunch {
