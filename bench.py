@@ -7,7 +7,8 @@ column-major, FP32 accumulation, BF16 output, algorithm chosen per shape by
 the library's cost model (``LCGEMM_AUTO``).  ``value`` is sum(2 n^3) over the
 sweep divided by the summed device time of the four GEMMs (CUDA events on the
 launching stream, L2 flushed by a 256 MB write before every timed launch,
-outside the event pair).  ``server`` repeats the launches with seeded random
+outside the event pair).  Offline timing is per shape: each size gets its W
+warm-up launches and then its K timed launches back to back, sizes ascending.  ``server`` repeats the launches with seeded random
 0-5 ms host sleeps in between (the randomly spaced launch mode), ``e2e``
 times the host-buffer entry point ``lcgemm_run_host`` with page-locked inputs
 (host->device copies, the GEMM and the device->host copy of C inside the
@@ -207,24 +208,27 @@ def run_gpu(args):
 
     evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for n in SIZES}
-    with ClockSampler(local) as clk:          # runs through warm-up and the timed region (samples under load)
-        for _ in range(args.warmup):
-            for n in SIZES:
+    # ---- offline, per shape (the offline protocol: warm-up runs of a shape, then its launches back
+    # to back): for each size, W untimed launches, then its K timed launches between a barrier and a
+    # synchronisation on both sides.  A step is one timed launch of every size, so the K steps are
+    # timed exactly, size by size; the sizes run in ascending order.
+    t_wall = 0.0
+    with ClockSampler(local) as clk:          # runs through warm-up and the timed launches (samples under load)
+        for n in SIZES:
+            for _ in range(args.warmup):
                 one(n)
-        torch.cuda.synchronize(dev)
-        rc = h.sync_status()
-        if rc:
-            raise RuntimeError(f"device status {rc} after warm-up")
-        # ---- offline: the K timed steps
-        _barrier(world)
-        torch.cuda.synchronize(dev)
-        t_wall0 = time.perf_counter()
-        for s in range(args.steps):
-            for n in SIZES:
+            torch.cuda.synchronize(dev)
+            rc = h.sync_status()
+            if rc:
+                raise RuntimeError(f"device status {rc} after warm-up")
+            _barrier(world)
+            torch.cuda.synchronize(dev)
+            t_wall0 = time.perf_counter()
+            for s in range(args.steps):
                 one(n, evs[n][s])
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall0
-        _barrier(world)
+            torch.cuda.synchronize(dev)
+            t_wall += time.perf_counter() - t_wall0
+            _barrier(world)
     rc = h.sync_status()
     if rc:
         raise RuntimeError(f"device status {rc} in the timed region")
@@ -287,8 +291,10 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD, "sizes": list(SIZES), "algo": "auto",
                        "chosen": {str(n): chosen[n] for n in SIZES}, "parallelism": f"replicas x{world}",
                        "l2": "flushed (256 MB write) before every timed launch; inputs >= 8192^3 exceed L2",
-                       "timing": "CUDA events around each launch on the launching stream; a ~0.2 ms device-side "
-                                 "wait after the flush covers the host's submission of the GEMM"},
+                       "timing": "offline, per size in ascending order: W warm-up launches, then the K timed "
+                                 "launches back to back between barrier + synchronize brackets; CUDA events around "
+                                 "each launch on the launching stream; a ~0.2 ms device-side wait after the flush "
+                                 "covers the host's submission of the GEMM"},
             "pct_of_peak": round(value / world / peak_burst, 4),
             "per_size": {str(n): {"algo": chosen[n], "median_ms": round(statistics.median(per_n_ms[n]), 4),
                                   "tflops": round(2.0 * n ** 3 / (statistics.median(per_n_ms[n]) * 1e-3) / 1e12, 1),
