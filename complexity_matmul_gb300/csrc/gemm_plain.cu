@@ -291,6 +291,10 @@ constexpr int kReducePer = 32 * kBM / kReduceThreads;   // elements per thread (
 template <int BN, bool BF16>
 __global__ void __launch_bounds__(kReduceThreads) splitk_reduce_kernel(const PlainArgs a) {
   __shared__ float T[32][kBM + 1];
+  // launched as a programmatic dependent of the GEMM that wrote the partials: its blocks
+  // are resident when that grid ends and read nothing before it has completed
+  griddep_launch_dependents();
+  griddep_wait();
   constexpr int kChunks = BN / 32;
   const int tile = blockIdx.x / kChunks;
   const int c32 = (blockIdx.x % kChunks) * 32;
@@ -362,8 +366,8 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
 template <int BN, bool BF16>
 cudaError_t launch_reduce_impl(const PlainLaunch& L, cudaStream_t stream) {
   const int64_t blocks = int64_t(L.args.num_tiles) * (BN / 32);
-  splitk_reduce_kernel<BN, BF16><<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(L.args);
-  return cudaGetLastError();
+  return launch_maybe_pdl(splitk_reduce_kernel<BN, BF16>, static_cast<int>(blocks), kReduceThreads, 0, stream, L.pdl,
+                          L.args);
 }
 
 }  // namespace
