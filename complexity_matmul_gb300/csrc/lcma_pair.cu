@@ -288,6 +288,29 @@ __device__ __forceinline__ void tile_coords_l2(int t, const LcmaArgs& a, int& mb
   nb = local / rows;
 }
 
+// The quadrant scratch is read back within a few products: its stores and loads
+// carry an L2 evict-last policy so that the operand panels streaming through L2
+// push it out last; lines of a slot that is dead until the next Group rewrites
+// it are dropped without a write-back (discard), by lane 0 of the warp that owns
+// them, between two __syncwarp barriers (the warp's loads of them are complete
+// before, and its later stores to them come after).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_keep(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ float ld_keep(const float* p, uint64_t pol) {
+  float v;
+  asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol) : "memory");
+  return v;
+}
+__device__ __forceinline__ void discard_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Two levels: 32 FP32 values (one row, columns qcol .. qcol+31) of inner
 // quadrant `iq` of this launch's outer product P go to the outer level: into an
 // outer slot (Init / Acc), or, with the slot's sum, into outer quadrant q of C
@@ -336,8 +359,9 @@ __device__ __forceinline__ void apply_outer(const float (&v)[32], int iq, int rl
 template <bool BF16>
 __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st, float* scratch, int row,
                                                 const LcmaArgs& a, int rloc, int col0, int tile_col0,
-                                                const float* partner) {
+                                                const float* partner, bool last_step) {
   uint16_t* Cp = static_cast<uint16_t*>(a.C);
+  const uint64_t pol = l2_policy_evict_last();
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t r[32];
@@ -352,13 +376,13 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
       const float sg = static_cast<float>(t.sign);
       if (t.kind == kTgtInit) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sp[j * kRows] = sg * __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) st_keep(sp + j * kRows, sg * __uint_as_float(r[j]), pol);
       } else if (t.kind == kTgtAcc) {
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows];
+        for (int j = 0; j < 32; ++j) v[j] = ld_keep(sp + j * kRows, pol);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sp[j * kRows] = v[j] + sg * __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) st_keep(sp + j * kRows, v[j] + sg * __uint_as_float(r[j]), pol);
       } else {
         float v[32];
         if (t.kind == kTgtFinalPX) {
@@ -366,15 +390,25 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
           for (int j = 0; j < 32; ++j) v[j] = sg * __uint_as_float(r[j]);
         } else if (t.kind == kTgtFinalSX) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows];
+          for (int j = 0; j < 32; ++j) v[j] = ld_keep(sp + j * kRows, pol);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = sp[j * kRows] + sg * __uint_as_float(r[j]);
+          for (int j = 0; j < 32; ++j) v[j] = ld_keep(sp + j * kRows, pol) + sg * __uint_as_float(r[j]);
         }
         if (t.kind == kTgtFinalPX || t.kind == kTgtFinalSX) {
           const float* pp = partner + (static_cast<int64_t>(t.slot) * kTileN + col) * kRows + row;
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += __ldcg(pp + j * kRows);
+        }
+        if (last_step && t.kind != kTgtFinalPX) {
+          // the slot is dead until the next Group writes it again
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) {
+            const float* line = sp - (row & 31);     // this warp's 32 rows of column col
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j) discard_line(line + j * kRows);
+          }
+          __syncwarp();
         }
         const int qcol = tile_col0 + col;              // column inside the quadrant
         if (a.outer) {
@@ -573,8 +607,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const uint32_t tsrc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + half * 128;
+        // at the last step of a whole Group, the slots it reads are dead until the next Group
         consume_product<BF16>(tsrc, d_l2_programs[type][s], scratch, row, args_in, rloc, half * 128, nb * kTileN,
-                              partner);
+                              partner, s == nsteps - 1 && (type == kItemFull || type == kItemFullMixed));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&pempty[buf]), 0));
