@@ -12,7 +12,10 @@
  *                combine / product / recombine pipeline and its fusion are in
  *                section "从 LCMA 到 FalconGEMM").
  *   - strassen2: two-level Strassen, 49 block products over a 4x4 block grid
- *                (same section: 49 instead of 64 block multiplications).
+ *                (same section: 49 instead of 64 block multiplications); the
+ *                seven outer products each run as one pass of the fused
+ *                one-level kernel over the inner blocks, and the outer level
+ *                is combined in FP32 before the one cast.
  *   - auto:      a roofline-style cost model picks one of the above per shape
  *                (section "从缓存重排到 Cost Model").
  * The one-level scheme is the textbook Strassen (1969) formulas:
@@ -76,7 +79,7 @@ enum { LCGEMM_F16 = 0, LCGEMM_BF16 = 1 };
 enum {
   LCGEMM_PLAIN = 0,             /* persistent tiled GEMM                                  */
   LCGEMM_STRASSEN1 = 1,         /* one-level Strassen: combine pre-pass + fused products  */
-  LCGEMM_STRASSEN2 = 2,         /* two-level Strassen (49 products)                       */
+  LCGEMM_STRASSEN2 = 2,         /* two-level Strassen (49 products, fused hierarchically) */
   LCGEMM_AUTO = 3,              /* cost model chooses among the three above               */
   LCGEMM_STRASSEN1_UNFUSED = 4  /* ablation: combine, 7 products written to HBM in FP32,
                                    separate recombination kernel (the basic pipeline)     */
