@@ -312,3 +312,40 @@ def test_group_order_on_off(hp, M, N, K):
         out[order] = _run(hp, An, Bn, "strassen1").cpu()
     hp.set_option(lcg.OPT_GROUP_ORDER, 1)
     assert torch.equal(out[0], out[1])
+
+
+@pytest.mark.parametrize("split", [1, 0])
+@pytest.mark.parametrize("order", [1, 0])
+def test_two_level_hierarchical_options(hp, split, order):
+    """Two levels on the CTA-pair kernel run as seven launches (one per outer product) whose inner
+    quadrants go to FP32 outer slots: exact on integer inputs with the tail split and the Group
+    ordering on or off (each launch's 4 Groups form a tail that is split), and for a ragged shape
+    whose inner blocks are not multiples of the 256 x 256 Group tile."""
+    hp.set_option(lcg.OPT_SPLIT, split)
+    hp.set_option(lcg.OPT_GROUP_ORDER, order)
+    for (M, N, K) in ((2048, 2048, 1024), (1160, 1096, 544)):
+        A, B = synthetic.operands(M, N, K, "int3", 17, "bf16", "cuda")
+        assert_bit_exact(_run(hp, A, B, "strassen2"), oracle_c64(A, B, "bf16"), "bf16")
+    hp.set_option(lcg.OPT_SPLIT, 1)
+    hp.set_option(lcg.OPT_GROUP_ORDER, 1)
+
+
+def test_two_level_partner_timeout_is_reported_and_recovered():
+    """The split-Group fix-up inside the seven two-level launches: second halves that never publish
+    make the first halves' bounded waits run out; the status reports LCGEMM_ERR_TIMEOUT once and the
+    next run is exact."""
+    h2 = lcg.Handle(0)
+    h2.set_option(lcg.OPT_LCMA_KERNEL, 2)
+    h2.set_option(lcg.OPT_WAIT_TIMEOUT_US, 50000)
+    A, B = synthetic.operands(2048, 2048, 1024, "int3", 18, "bf16", "cuda")
+    h2.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 1)
+    h2.run(A, B, algo="strassen2")
+    torch.cuda.synchronize()
+    assert h2.sync_status() == lcg.ERR_TIMEOUT
+    assert h2.sync_status() == lcg.OK
+    h2.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 0)
+    C = h2.run(A, B, algo="strassen2")
+    torch.cuda.synchronize()
+    assert h2.sync_status() == lcg.OK
+    assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
+    h2.close()
