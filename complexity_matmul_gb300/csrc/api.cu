@@ -376,6 +376,13 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
       if (cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     }
     L.grid = 2 * static_cast<int>(std::min<int64_t>(a.num_items, P));
+    // many waves: claimed items (the counter starts at zero; a memset before each
+    // launch also covers a launch that aborted and graph replays)
+    a.tile_ctr = nullptr;
+    if (a.num_items >= kPairClaimMinWaves * P) {
+      if (cudaMemsetAsync(h->tile_ctr, 0, sizeof(int), st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+      a.tile_ctr = h->tile_ctr;
+    }
     return launch_plain_pair(L, st) == cudaSuccess ? LCGEMM_OK : LCGEMM_ERR_CUDA;
   }
   L.grid = static_cast<int>(std::min<int64_t>(tiles * a.splits, grid_cap(h)));
@@ -423,6 +430,12 @@ int lcgemm_create(lcgemm_t* out, int device) {
     delete h;
     return LCGEMM_ERR_CUDA;
   }
+  if (cudaMalloc(&h->tile_ctr, 256) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeHost(h->err_host);
+    delete h;
+    return LCGEMM_ERR_NOMEM;
+  }
   if (const char* s = std::getenv("LCGEMM_PEAK_GFLOPS")) {
     const double v = std::atof(s);
     if (v > 0) h->peak_gflops = v;
@@ -447,6 +460,7 @@ int lcgemm_destroy(lcgemm_t h) {
   if (h->stage) cudaFree(h->stage);
   if (h->skinny_ctr) cudaFree(h->skinny_ctr);
   if (h->pad) cudaFree(h->pad);
+  if (h->tile_ctr) cudaFree(h->tile_ctr);
   for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
   if (h->copy_in) cudaStreamDestroy(h->copy_in);
   if (h->copy_out) cudaStreamDestroy(h->copy_out);

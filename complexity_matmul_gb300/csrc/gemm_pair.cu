@@ -13,12 +13,26 @@
 // partial and the second half to finish adds both (in half order) and casts.
 // Nobody waits for anybody.
 //
+// Work distribution.  Few waves: pair p runs items p, p + P, p + 2P, ... (P
+// pairs).  Many waves (DYN): every pair still starts with item p, but takes
+// each later item from a global counter, claimed a few slabs before its
+// current item ends.  Claims then follow the order in which pairs become free,
+// so the items that share an A or B panel (neighbours in the grouped raster)
+// run close together in time whatever the pairs' drift, and the panel is still
+// in L2 for the second reader: at 16384^3 this halves the DRAM reads of the
+// static order.  The leader CTA's producer claims and publishes each item
+// through a small queue in both CTAs' shared memory; the other roles read it
+// from there.  The host zeroes the counter before each such launch.
+//
 // Synchronisation across the pair:
 //   full[s]   leader's barrier; the leader arms it with both CTAs' bytes and
 //             both CTAs' TMA copies complete on it
 //   empty[s]  one per CTA; the leader's MMA commit arrives on both
 //   tfull[b]  one per CTA; the leader's MMA commit arrives on both
 //   tempty[b] leader's barrier; all 8 epilogue warps of the pair arrive
+//   qfull[j]  one per CTA (DYN); the leader's producer arrives after writing
+//             queue slot j of that CTA
+//   qempty[j] leader's barrier (DYN); every reader of slot j arrives
 #include "kernels.h"
 #include "plain_common.cuh"
 #include "ptx.cuh"
@@ -37,7 +51,44 @@ constexpr int kBBytes = (kBN / 2) * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTxBytes = 2 * kStageBytes;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr int kQ = 4;              // queue slots (DYN): items published but not yet read by every role
+constexpr int kQReaders = 10;      // the leader's MMA issuer, the partner's producer, 8 epilogue warps
+constexpr int kClaimLead = 8;      // the next item is claimed this many slabs before the current one ends
+constexpr int kSmemBytes = kStages * kStageBytes + 512 + 1024;
+
+// Queue of claimed items (DYN).  `item`/`full` are this CTA's; `empty` is the
+// leader CTA's (addressed through the cluster window from either CTA).
+struct ItemQueue {
+  int* item;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t slot, phase;
+
+  __device__ __forceinline__ void advance() {
+    if (++slot == kQ) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+  // Leader's producer: writes item w into slot `slot` of both CTAs and signals them.
+  __device__ __forceinline__ bool publish(int w, const WaitCtl& wc) {
+    if (!mbar_wait_cluster(&empty[slot], phase ^ 1, wc)) return false;
+    item[slot] = w;
+    st_relaxed_cluster_s32(mapa_shared(smem_u32(&item[slot]), 1), w);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&full[slot]), 0));
+    mbar_arrive_cluster(mapa_shared(smem_u32(&full[slot]), 1));
+    advance();
+    return true;
+  }
+  // Any other role: reads the next item and frees the slot.
+  __device__ __forceinline__ bool pop(int& w, const WaitCtl& wc) {
+    if (!mbar_wait_cluster(&full[slot], phase, wc)) return false;
+    w = *reinterpret_cast<volatile int*>(&item[slot]);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&empty[slot]), 0));
+    advance();
+    return true;
+  }
+};
 
 // Work item -> tile and K-slab range.  Items below tail_first are whole tiles;
 // the rest are the two K halves of the tiles of the partial last wave.
@@ -58,7 +109,7 @@ __device__ __forceinline__ void pair_item(int w, const PlainArgs& a, int num_kb,
   }
 }
 
-template <bool BF16, bool EPI>
+template <bool BF16, bool EPI, bool DYN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     plain_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const PlainArgs args) {
@@ -72,7 +123,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* qfull = drain + 1;
+  uint64_t* qempty = qfull + kQ;
+  int* qitem = reinterpret_cast<int*>(qempty + kQ);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qitem + kQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -90,6 +144,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[b], 8);
     }
     mbar_init(drain, 1);
+    for (int j = 0; j < kQ; ++j) {
+      mbar_init(&qfull[j], 1);
+      mbar_init(&qempty[j], kQReaders);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -109,18 +167,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int num_kb = (args.K + kBK - 1) / kBK;
   const int pair = blockIdx.x / 2;
   const int num_pairs = gridDim.x / 2;
+  ItemQueue iq{qitem, qfull, qempty, 0, 0};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int w = pair; ok && w < args.num_items; w += num_pairs) {
+      int next = pair;   // DYN leader: the item claimed for after the current one
+      for (int w = pair; ok;) {
+        if constexpr (DYN) {
+          if (leader) {
+            w = next;
+            if (!iq.publish(w, wc)) {
+              ok = false;
+              break;
+            }
+          } else if (!iq.pop(w, wc)) {
+            ok = false;
+            break;
+          }
+        }
+        if (w >= args.num_items) break;   // DYN: every pair's last claim lies past the end
         int tile, kb0, kb1, half;
         pair_item(w, args, num_kb, tile, kb0, kb1, half);
         int mb, nb;
         tile_coords(tile, args, mb, nb);
+        const int claim_at = max(kb0, kb1 - kClaimLead);
         for (int kb = kb0; kb < kb1; ++kb) {
+          if (DYN && leader && kb == claim_at) next = num_pairs + atomicAdd(args.tile_ctr, 1);
           if (!mbar_wait(&empty[stage], phase ^ 1, wc)) {
             ok = false;
             break;
@@ -136,6 +211,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             phase ^= 1;
           }
         }
+        if (DYN && leader && kb0 >= kb1) next = num_pairs + atomicAdd(args.tile_ctr, 1);   // (no empty items exist)
+        if constexpr (!DYN) w += num_pairs;
       }
       if (!ok) {
         // Aborting: let this CTA's copies land before it leaves.
@@ -155,7 +232,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      for (int w = pair; ok && w < args.num_items; w += num_pairs) {
+      for (int w = pair; ok; w += num_pairs) {
+        if constexpr (DYN) {
+          if (!iq.pop(w, wc)) break;
+        }
+        if (w >= args.num_items) break;
         int tile, kb0, kb1, half;
         pair_item(w, args, num_kb, tile, kb0, kb1, half);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, wc)) {
@@ -198,7 +279,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
     uint16_t* Cp = static_cast<uint16_t*>(args.C);
-    for (int w = pair; w < args.num_items; w += num_pairs) {
+    for (int w = pair;; w += num_pairs) {
+      if constexpr (DYN) {
+        int v = 0;
+        const bool got = lane == 0 ? iq.pop(v, wc) : true;
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) break;
+        w = __shfl_sync(0xffffffffu, v, 0);
+      }
+      if (w >= args.num_items) break;
       int tile, kb0, kb1, half;
       pair_item(w, args, num_kb, tile, kb0, kb1, half);
       int mb, nb;
@@ -289,9 +377,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16, bool EPI>
+template <bool BF16, bool EPI, bool DYN>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
-  auto kern = plain_pair_kernel<BF16, EPI>;
+  auto kern = plain_pair_kernel<BF16, EPI, DYN>;
   {
     const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -304,8 +392,12 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream) {
   if (L.grid % 2) return cudaErrorInvalidValue;
   // the kernel without an epilogue keeps the lean store path
-  if (L.args.ep.on) return L.bf16 ? launch_impl<true, true>(L, stream) : launch_impl<false, true>(L, stream);
-  return L.bf16 ? launch_impl<true, false>(L, stream) : launch_impl<false, false>(L, stream);
+  if (L.args.tile_ctr) {
+    if (L.args.ep.on) return L.bf16 ? launch_impl<true, true, true>(L, stream) : launch_impl<false, true, true>(L, stream);
+    return L.bf16 ? launch_impl<true, false, true>(L, stream) : launch_impl<false, false, true>(L, stream);
+  }
+  if (L.args.ep.on) return L.bf16 ? launch_impl<true, true, false>(L, stream) : launch_impl<false, true, false>(L, stream);
+  return L.bf16 ? launch_impl<true, false, false>(L, stream) : launch_impl<false, false, false>(L, stream);
 }
 
 }  // namespace lcg

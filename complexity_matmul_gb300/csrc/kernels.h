@@ -46,6 +46,9 @@ struct PlainArgs {
   // counters [tile][rank][4]).
   int tail_first;
   int num_items;
+  // CTA-pair kernel, many waves: items after each pair's first are claimed from
+  // this counter (zero at launch); null: the static order
+  int* tile_ctr;
   Epilogue ep;
   // split-K with many chunks: the chunks only publish their partials and a
   // separate reduction kernel sums them (every output element in parallel)
@@ -87,6 +90,9 @@ cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream);
 // halves (partials through L2, a counter, the later half's sum) costs a few
 // microseconds, which only long enough tiles win back.
 constexpr int kTailSplitMinSlabs = 96;
+// From this many waves of items on, the pair kernel claims items dynamically
+// (DRAM re-reads of the static order grow with the drift between pairs).
+constexpr int kPairClaimMinWaves = 16;
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 
 // Skinny GEMM (M <= 256): C^T = B . A^T with 128-row blocks of B as the MMA's

@@ -350,6 +350,40 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
+__device__ __forceinline__ void st_relaxed_cluster_s32(uint32_t addr_cluster, int v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.s32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_acquire_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for a barrier that the other CTA of the cluster arrives on with
+// release semantics: the wait acquires at cluster scope, so what that CTA wrote
+// before arriving (e.g. into this CTA's shared memory) is visible afterwards.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_try_wait_acquire_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_acquire_cluster(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        record_error(w, kErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_cluster_u32(uint32_t addr_cluster) {
   uint32_t v;
   asm volatile("ld.acquire.cluster.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr_cluster) : "memory");

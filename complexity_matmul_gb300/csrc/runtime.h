@@ -12,6 +12,7 @@ struct lcgemm_ctx {
   int num_sms = 0;
   int* err_host = nullptr;   // mapped, page-locked error word (host view)
   int* err_dev = nullptr;    // the same word as the device sees it
+  int* tile_ctr = nullptr;   // CTA-pair kernel's item counter (device)
   uint64_t timeout_ns = 2000000000ull;
   int group_order = 1;
   int split = 1;

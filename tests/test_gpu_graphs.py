@@ -77,3 +77,31 @@ def test_capture_refuses_buffer_growth():
     torch.cuda.synchronize()
     assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
     h.close()
+
+
+def test_capture_claimed_items():
+    """The CTA-pair kernel's claimed-item path (8 CTAs, 64 tiles = 16 waves): the counter's reset is
+    part of the graph, so every replay runs every tile once."""
+    M = N = 2048
+    K = 512
+    h = lcg.Handle(0)
+    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    h.set_option(lcg.OPT_MAX_CTAS, 8)
+    A, B = synthetic.operands(M, N, K, "int3", 95, "bf16", "cuda")
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    h.run(A, B, C, algo="plain")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        h.run(A, B, C, algo="plain")
+    for seed in (96, 97):
+        A2, B2 = synthetic.operands(M, N, K, "int3", seed, "bf16", "cuda")
+        A.copy_(A2)
+        B.copy_(B2)
+        C.fill_(0)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        assert h.sync_status() == 0
+        assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
+    h.close()

@@ -7,7 +7,7 @@ import torch
 
 import complexity_matmul_gb300 as lcg
 import synthetic
-from helpers import assert_bit_exact, assert_close, oracle_c64, oracle_epilogue, padded
+from helpers import assert_bit_exact, assert_close, assert_epilogue_close, oracle_c64, oracle_epilogue, padded
 
 pytestmark = pytest.mark.gpu
 
@@ -276,4 +276,56 @@ def test_one_row_96_column_tiles(M, N, K):
         torch.cuda.synchronize()
         assert h.sync_status() == 0
         assert_bit_exact(C, D64, "bf16")
+    h.close()
+
+
+# ---------------------------------------------------------------- claimed items (CTA-pair kernel, many waves)
+
+@pytest.mark.parametrize("ctas,M,N,K,dtype", [(8, 2048, 2048, 512, "bf16"), (8, 1900, 2100, 700, "f16"),
+                                              (16, 2560, 3328, 6144, "bf16")])
+def test_claimed_items_bit_exact(ctas, M, N, K, dtype):
+    """With at least 16 waves of items the CTA-pair kernel claims every pair's later items from a
+    counter.  A cap of 8 or 16 CTAs (4 or 8 pairs) puts small shapes there: exactly 16 waves, a
+    ragged edge, and 130 tiles with the tail split (16 full waves + 2 tiles as K halves).  Integer
+    inputs bit-exact against the oracle, the same bits as the static order on the full machine, and
+    stable over back-to-back launches (the counter starts from zero each time)."""
+    A, B = synthetic.operands(M, N, K, "int3", 81, dtype, "cuda")
+    rows = None if M * N * K <= 4e9 else synthetic.row_sample(M, 256)
+    ref = oracle_c64(A, B, dtype, rows=rows)
+    A, B = padded(M, K, dtype, A), padded(N, K, dtype, B)   # 16-byte row starts for any K
+    h = lcg.Handle(0)
+    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    h.set_option(lcg.OPT_MAX_CTAS, ctas)
+    Cs = [h.run(A, B, algo="plain") for _ in range(4)]
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    assert_bit_exact(Cs[0], ref, dtype, rows=rows)
+    assert all(torch.equal(Cs[0], C) for C in Cs[1:])
+    full = lcg.Handle(0)
+    full.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    assert torch.equal(_run(full, A, B), Cs[0])
+    full.close()
+    h.close()
+
+
+def test_claimed_items_with_epilogue():
+    """The fused epilogue on claimed items (bias, residual, GELU; exact integer product) against the
+    oracle's FP64 D, and the same bits as the static order."""
+    M, N, K = 1792, 2304, 640
+    A, B = synthetic.operands(M, N, K, "int3", 82, "bf16", "cuda")
+    b = synthetic.matrix(1, N, "int3", 83, "bf16", "cuda")[0]
+    R = synthetic.matrix(M, N, "int3", 84, "bf16", "cuda")
+    D64, pre = oracle_epilogue(A, B, "bf16", b, R, "gelu")
+    h = lcg.Handle(0)
+    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    h.set_option(lcg.OPT_MAX_CTAS, 8)
+    C = h.run(A, B, algo="plain", bias=b, residual=R, act="gelu")
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    assert_epilogue_close(C, D64, pre, "bf16", "gelu")
+    h.set_option(lcg.OPT_MAX_CTAS, 0)
+    C2 = h.run(A, B, algo="plain", bias=b, residual=R, act="gelu")
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    assert torch.equal(C, C2)
     h.close()
