@@ -36,7 +36,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
-                const uint64_t* strides_bytes, const uint32_t* box) {
+                const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5];
@@ -51,7 +51,7 @@ bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uin
   }
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -358,6 +358,12 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     }
   }
   if (pair) {
+    // C for the tensor stores of whole tiles: 32 x 32 boxes (one epilogue warp's
+    // chunk), 64-byte swizzle in shared memory
+    const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t cstrides[1] = {static_cast<uint64_t>(ldc) * 2};
+    const uint32_t cbox[2] = {32u, 32u};
+    if (!encode_map(&L.tmC, bf16, C, 2, cdims, cstrides, cbox, CU_TENSOR_MAP_SWIZZLE_64B)) return LCGEMM_ERR_CUDA;
     // split the partial last wave into K halves when its tiles fit twice over
     const int P = grid_cap(h) / 2;
     const int full = a.num_tiles / P, rem = a.num_tiles - full * P;

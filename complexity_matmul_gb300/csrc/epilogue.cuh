@@ -177,12 +177,12 @@ __device__ __forceinline__ void cast_store(uint16_t* dst, int n, const float (&v
   }
 }
 
-// Epilogue + cast + store of v[0 .. n) = C[row, col .. col + n) (n <= W; the
-// values past n are ignored).  dst points at C[row, col].  `pre`: this run's
+// The epilogue act(v + bias) + residual, in place, of v[0 .. n) = C[row, col ..
+// col + n) (n <= W; the values past n are left as they are).  `pre`: this run's
 // bias / residual words if epilogue_load() fetched them, else null.
 template <bool BF16, int W>
-__device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t col, int n, float (&v)[W],
-                                          const Epilogue& e, const EpiLoads<W>* pre = nullptr) {
+__device__ __forceinline__ void apply_epilogue(int64_t row, int64_t col, int n, float (&v)[W], const Epilogue& e,
+                                               const EpiLoads<W>* pre = nullptr) {
   const bool full = n == W;
   if (e.on) {
     if (e.bias) {
@@ -213,6 +213,13 @@ __device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t co
       }
     }
   }
+}
+
+// Epilogue + cast + store of v[0 .. n) = C[row, col .. col + n); dst points at C[row, col].
+template <bool BF16, int W>
+__device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t col, int n, float (&v)[W],
+                                          const Epilogue& e, const EpiLoads<W>* pre = nullptr) {
+  apply_epilogue<BF16, W>(row, col, n, v, e, pre);
   cast_store<BF16, W>(dst, n, v);
 }
 

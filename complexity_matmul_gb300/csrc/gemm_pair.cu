@@ -54,7 +54,25 @@ constexpr int kTmemCols = 2 * kBN;
 constexpr int kQ = 4;              // queue slots (DYN): items published but not yet read by every role
 constexpr int kQReaders = 10;      // the leader's MMA issuer, the partner's producer, 8 epilogue warps
 constexpr int kClaimLead = 8;      // the next item is claimed this many slabs before the current one ends
-constexpr int kSmemBytes = kStages * kStageBytes + 512 + 1024;
+constexpr int kCBoxBytes = 32 * 32 * 2;            // one epilogue warp's 32 x 32 chunk of C
+constexpr int kCStageBytes = 4 * 2 * kCBoxBytes;     // two boxes per epilogue warp
+constexpr int kSmemBytes = kStages * kStageBytes + kCStageBytes + 512 + 1024;
+
+// Cast of one 32 x 32 chunk (lane = row, v = its 32 columns) into a shared-memory
+// box of 32 rows x 64 bytes laid out in the tensor map's 64-byte swizzle: 16-byte
+// unit j of row r at r * 64 + (j ^ ((r >> 1) & 3)) * 16, so that the warp's
+// stores of one unit hit every bank once per quarter warp.
+template <bool BF16>
+__device__ __forceinline__ void stage_chunk(uint32_t box, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t addr = box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pack2(v[8 * j], v[8 * j + 1], BF16)),
+                 "r"(pack2(v[8 * j + 2], v[8 * j + 3], BF16)), "r"(pack2(v[8 * j + 4], v[8 * j + 5], BF16)),
+                 "r"(pack2(v[8 * j + 6], v[8 * j + 7], BF16))
+                 : "memory");
+  }
+}
 
 // Queue of claimed items (DYN).  `item`/`full` are this CTA's; `empty` is the
 // leader CTA's (addressed through the cluster window from either CTA).
@@ -112,12 +130,13 @@ __device__ __forceinline__ void pair_item(int w, const PlainArgs& a, int num_kb,
 template <bool BF16, bool EPI, bool DYN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     plain_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const PlainArgs args) {
+                      const __grid_constant__ CUtensorMap tmC, const PlainArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sC = sB + kStages * kBBytes;   // epilogue boxes (1024-byte aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + kCStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -297,26 +316,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
       if (half < 0) {
-        if constexpr (EPI) {
-          // the next chunk's bias / residual loads are in flight while this chunk is finished
-          EpiLoads<32> pre;
-          load_chunk(row, nb * kBN, args, pre);
+        // whole tile: each 32 x 32 chunk is finished in registers, cast into one of
+        // the warp's two shared-memory boxes and written by a tensor store (full
+        // lines; rows and columns past C are clipped by the tensor map)
+        const int row0 = row - lane;
+        EpiLoads<32> pre;
+        if constexpr (EPI) load_chunk(row, nb * kBN, args, pre);   // next chunk's bias / residual in flight
 #pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c * 32, r);
-            const EpiLoads<32> cur = pre;
-            if (c + 1 < kBN / 32) load_chunk(row, nb * kBN + (c + 1) * 32, args, pre);
-            tmem_wait_ld();
-            store_chunk<BF16, true>(crow, row, nb * kBN + c * 32, r, args, &cur);
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col = nb * kBN + c * 32;
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          EpiLoads<32> cur;
+          if constexpr (EPI) {
+            cur = pre;
+            if (c + 1 < kBN / 32) load_chunk(row, col + 32, args, pre);
           }
-        } else {
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c * 32, r);
-            tmem_wait_ld();
-            store_chunk<BF16, false>(crow, row, nb * kBN + c * 32, r, args);
+          tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          if constexpr (EPI)
+            if (row < args.M && col < args.N) apply_epilogue<BF16, 32>(row, col, min(32, args.N - col), v, args.ep, &cur);
+          const uint32_t box = smem_u32(sC) + (q * 2 + (c & 1)) * kCBoxBytes;
+          if (lane == 0) bulk_wait_read<1>();   // the store that read this box two chunks ago is done with it
+          __syncwarp();
+          stage_chunk<BF16>(box, lane, v);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            if (row0 < args.M && col < args.N) tma_store_2d(&tmC, box, col, row0);
+            bulk_commit();
           }
         }
         tc_fence_before();
@@ -367,6 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_all();   // the tensor stores have read their boxes and written C
   }
 
   tc_fence_before();
@@ -384,7 +415,7 @@ cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
     const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes);
     if (e != cudaSuccess) return e;
   }
-  return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
+  return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.tmC, L.args);
 }
 
 }  // namespace

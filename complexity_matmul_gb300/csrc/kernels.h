@@ -65,6 +65,7 @@ struct PlainArgs {
 
 struct PlainLaunch {
   CUtensorMap tmA, tmB;
+  CUtensorMap tmC;      // CTA-pair kernel: C in 32 x 32 boxes, 64-byte swizzle (tensor stores)
   PlainArgs args;
   int bn;               // 128 or 256
   bool bf16;

@@ -42,7 +42,8 @@ struct lcgemm_ctx {
 namespace lcg {
 
 bool encode_map(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
-                const uint64_t* strides_bytes, const uint32_t* box);
+                const uint64_t* strides_bytes, const uint32_t* box,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 bool encode_kmajor(CUtensorMap* m, bool bf16, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows);
 int grid_cap(const lcgemm_ctx* h);
 int plain_single_bn(int64_t M, int64_t N, int sms);
