@@ -8,6 +8,11 @@
 // reads 16 KB of A and 8 KB of (its half of) B per 64-deep K slab instead of
 // 16 KB + 32 KB, which halves the shared-memory and L2 traffic per flop.
 //
+// Epilogue: each warp casts 32 x 32 chunks of its 32 accumulator rows into two
+// alternating shared-memory boxes and writes each with one tensor store, so C
+// leaves in whole cache lines (a direct store of the row-per-lane layout
+// touches 32 lines per warp instruction, ~2 us per 256 x 256 tile).
+//
 // Tail split: when the tiles of the partial last wave fit twice over into the
 // pairs, each runs as two K halves on two pairs; each half publishes its FP32
 // partial and the second half to finish adds both (in half order) and casts.
