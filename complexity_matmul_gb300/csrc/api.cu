@@ -364,17 +364,20 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     const uint64_t cstrides[1] = {static_cast<uint64_t>(ldc) * 2};
     const uint32_t cbox[2] = {32u, 32u};
     if (!encode_map(&L.tmC, bf16, C, 2, cdims, cstrides, cbox, CU_TENSOR_MAP_SWIZZLE_64B)) return LCGEMM_ERR_CUDA;
-    // split the partial last wave into K halves when its tiles fit twice over
+    // many waves: claimed items; else the partial last wave runs as K halves when
+    // its tiles fit twice over
     const int P = grid_cap(h) / 2;
+    const bool claimed = a.num_tiles >= kPairClaimMinWaves * P;
     const int full = a.num_tiles / P, rem = a.num_tiles - full * P;
     const int num_kb = static_cast<int>((K + kPlainBK - 1) / kPlainBK);
-    const bool split = h->split && rem > 0 && 2 * rem <= P && num_kb >= kTailSplitMinSlabs;
+    const bool split = !claimed && h->split && rem > 0 && 2 * rem <= P && num_kb >= kTailSplitMinSlabs;
     a.tail_first = split ? full * P : a.num_tiles;
     a.num_items = split ? full * P + 2 * rem : a.num_tiles;
+    a.debug_drop = h->debug_drop;
     if (split) {
-      const size_t part_bytes = static_cast<size_t>(rem) * 2 * 256 * 256 * sizeof(float);
+      const size_t part_bytes = static_cast<size_t>(rem) * 2 * 256 * 128 * sizeof(float);
       const size_t off = (part_bytes + 255) / 256 * 256;
-      const size_t ctr_bytes = static_cast<size_t>(rem) * 2 * 4 * sizeof(int);
+      const size_t ctr_bytes = static_cast<size_t>(rem) * 2 * 2 * 4 * sizeof(int);
       int rc = ensure_workspace(h, off + ctr_bytes, st);
       if (rc) return rc;
       a.partial = static_cast<float*>(h->ws);
@@ -382,10 +385,10 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
       if (cudaMemsetAsync(a.counters, 0, ctr_bytes, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
     }
     L.grid = 2 * static_cast<int>(std::min<int64_t>(a.num_items, P));
-    // many waves: claimed items (the counter starts at zero; a memset before each
-    // launch also covers a launch that aborted and graph replays)
+    // claimed items: the counter starts at zero (a memset before each launch also
+    // covers a launch that aborted, and graph replays)
     a.tile_ctr = nullptr;
-    if (a.num_items >= kPairClaimMinWaves * P) {
+    if (claimed) {
       if (cudaMemsetAsync(h->tile_ctr, 0, sizeof(int), st) != cudaSuccess) return LCGEMM_ERR_CUDA;
       a.tile_ctr = h->tile_ctr;
     }

@@ -13,10 +13,13 @@
 // leaves in whole cache lines (a direct store of the row-per-lane layout
 // touches 32 lines per warp instruction, ~2 us per 256 x 256 tile).
 //
-// Tail split: when the tiles of the partial last wave fit twice over into the
-// pairs, each runs as two K halves on two pairs; each half publishes its FP32
-// partial and the second half to finish adds both (in half order) and casts.
-// Nobody waits for anybody.
+// Tail split (static order only): when the tiles of the partial last wave fit
+// twice over into the pairs, each runs as two K halves on two pairs.  Each half
+// publishes the FP32 partial of the 128 columns the other half finishes, raises
+// its flag, waits (bounded) for the other's flag, and finishes its own 128
+// columns as (0 + half 0) + half 1 from its accumulator and the other's
+// partial.  A pair has at most one such item, its last, and publishes before it
+// waits, so the two halves cannot wait on each other in a cycle.
 //
 // Work distribution.  Few waves: pair p runs items p, p + P, p + 2P, ... (P
 // pairs).  Many waves (DYN): every pair still starts with item p, but takes
@@ -129,6 +132,25 @@ __device__ __forceinline__ void pair_item(int w, const PlainArgs& a, int num_kb,
     const int mid = num_kb / 2;
     kb0 = half ? mid : 0;
     kb1 = half ? num_kb : mid;
+  }
+}
+
+// Epilogue (EPI), cast and tensor store of one finished 32 x 32 chunk: rows
+// row0 .. row0 + 31 (this lane: row), columns col .. col + 31, through `box`, one
+// of the warp's two shared-memory boxes used in turn.
+template <bool BF16, bool EPI>
+__device__ __forceinline__ void emit_chunk(float (&v)[32], int row, int row0, int col, uint32_t box, int lane,
+                                           const CUtensorMap* tmC, const PlainArgs& args, const EpiLoads<32>* cur) {
+  if constexpr (EPI)
+    if (row < args.M && col < args.N) apply_epilogue<BF16, 32>(row, col, min(32, args.N - col), v, args.ep, cur);
+  if (lane == 0) bulk_wait_read<1>();   // the store that read this box two chunks ago is done with it
+  __syncwarp();
+  stage_chunk<BF16>(box, lane, v);
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    if (row0 < args.M && col < args.N) tma_store_2d(tmC, box, col, row0);
+    bulk_commit();
   }
 }
 
@@ -302,7 +324,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
-    uint16_t* Cp = static_cast<uint16_t*>(args.C);
+    const uint32_t sbox = smem_u32(sC) + q * 2 * kCBoxBytes;   // this warp's two boxes
+    uint32_t nbox = 0;
     for (int w = pair;; w += num_pairs) {
       if constexpr (DYN) {
         int v = 0;
@@ -318,13 +341,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int row = mb * 2 * kBM + rank * kBM + q * 32 + lane;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, wc))) break;
       tc_fence_after();
-      uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+      const int row0 = row - lane;
       if (half < 0) {
         // whole tile: each 32 x 32 chunk is finished in registers, cast into one of
         // the warp's two shared-memory boxes and written by a tensor store (full
         // lines; rows and columns past C are clipped by the tensor map)
-        const int row0 = row - lane;
         EpiLoads<32> pre;
         if constexpr (EPI) load_chunk(row, nb * kBN, args, pre);   // next chunk's bias / residual in flight
 #pragma unroll 1
@@ -341,64 +363,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          if constexpr (EPI)
-            if (row < args.M && col < args.N) apply_epilogue<BF16, 32>(row, col, min(32, args.N - col), v, args.ep, &cur);
-          const uint32_t box = smem_u32(sC) + (q * 2 + (c & 1)) * kCBoxBytes;
-          if (lane == 0) bulk_wait_read<1>();   // the store that read this box two chunks ago is done with it
-          __syncwarp();
-          stage_chunk<BF16>(box, lane, v);
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            if (row0 < args.M && col < args.N) tma_store_2d(&tmC, box, col, row0);
-            bulk_commit();
-          }
+          emit_chunk<BF16, EPI>(v, row, row0, col, sbox + ((nbox++ & 1u) * kCBoxBytes), lane, &tmC, args, &cur);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
       } else {
-        // tail tile: publish this K half's FP32 partial (column-major slot of both
-        // ranks' 256 rows: one cache line per warp store), free the accumulator, and
-        // let the second half to arrive (per tile, CTA rank and lane quarter) sum both
+        // tail tile, K half `half`: the partial of the other half's 128 columns goes
+        // out (column-major per half: one cache line per warp store), then this
+        // half's 128 columns are finished from its accumulator and the other's partial
         const int i = tile - args.tail_first;
         const int slot_rows = 2 * kBM;
-        const int64_t slot = int64_t(slot_rows) * kBN;
-        const int chunks = min(kBN / 32, (args.N - nb * kBN + 31) / 32);
+        const int64_t slot = int64_t(slot_rows) * (kBN / 2);
         const int64_t rloc = rank * kBM + q * 32 + lane;
-        float* mine = args.partial + (int64_t(i) * 2 + half) * slot + rloc;
+        const int own_c0 = half * (kBN / 2), other_c0 = (half ^ 1) * (kBN / 2);
+        const int left = args.N - nb * kBN;   // columns of C from this tile's first on
+        const int out_chunks = max(0, min(kBN / 64, (left - other_c0 + 31) / 32));
+        float* out = args.partial + (int64_t(i) * 2 + half) * slot + rloc;
 #pragma unroll 1
-        for (int c = 0; c < chunks; ++c) {
+        for (int c = 0; c < out_chunks; ++c) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_ld_32x32b_x32(tbase + other_c0 + c * 32, r);
           tmem_wait_ld();
-          if (row < args.M) publish_partial(mine + c * 32 * slot_rows, slot_rows, r);
+          if (row < args.M) publish_partial(out + c * 32 * slot_rows, slot_rows, r);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
         __threadfence();
         __syncwarp();
-        int* ctr = args.counters + (i * 2 + static_cast<int>(rank)) * 4 + q;
-        int prev = 0;
-        if (lane == 0) prev = atom_add_acq_rel(ctr, 1);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == 1) {
-          if (lane == 0) *ctr = 0;
-          __threadfence();
-          const float* first = args.partial + int64_t(i) * 2 * slot + rloc;
-          if (row < args.M) {
+        int* flag = args.counters + ((i * 2 + half) * 2 + static_cast<int>(rank)) * 4 + q;
+        const int* peer = args.counters + ((i * 2 + (half ^ 1)) * 2 + static_cast<int>(rank)) * 4 + q;
+        if (lane == 0 && !(args.debug_drop && half == 1)) red_release_gpu_add(flag, 1);
+        if (__all_sync(0xffffffffu, wait_flag(peer, 1, wc))) {
+          // rows past M read slot entries nobody wrote and are not stored
+          const float* in = args.partial + (int64_t(i) * 2 + (half ^ 1)) * slot + rloc;
+          const int own_chunks = max(0, min(kBN / 64, (left - own_c0 + 31) / 32));
+          float o[32];
+          if (own_chunks > 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __ldcg(in + j * slot_rows);
+          }
 #pragma unroll 1
-            for (int c = 0; c < chunks; ++c) {
-              EpiLoads<32> pre;
-              if constexpr (EPI) load_chunk(row, nb * kBN + c * 32, args, pre);
-              uint32_t r[32];
-              sum_partials<2>(first + c * 32 * slot_rows, slot_rows, slot, r);
-              store_chunk<BF16, EPI>(crow, row, nb * kBN + c * 32, r, args, &pre);
+          for (int c = 0; c < own_chunks; ++c) {
+            const int col = nb * kBN + own_c0 + c * 32;
+            EpiLoads<32> cur;
+            if constexpr (EPI) load_chunk(row, col, args, cur);
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + own_c0 + c * 32, r);
+            tmem_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float mine = __uint_as_float(r[j]);
+              v[j] = half == 0 ? (0.f + mine) + o[j] : (0.f + o[j]) + mine;
+            }
+            // the next chunk's loads go out before this one is emitted (after it with the
+            // fused epilogue, whose registers they would otherwise share)
+            if (!EPI && c + 1 < own_chunks) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __ldcg(in + ((c + 1) * 32 + j) * slot_rows);
+            }
+            emit_chunk<BF16, EPI>(v, row, row0, col, sbox + ((nbox++ & 1u) * kCBoxBytes), lane, &tmC, args, &cur);
+            if (EPI && c + 1 < own_chunks) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __ldcg(in + ((c + 1) * 32 + j) * slot_rows);
             }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -42,10 +42,11 @@ struct PlainArgs {
   int* counters;        // [num_tiles][4], zero before the launch
   // tail split (CTA-pair kernel only): work items below tail_first are whole tiles,
   // the 2 * (num_tiles - tail_first) items after them are K halves of the last tiles
-  // (partials in `partial` as [tile][half][256 columns][256 rows], row fastest;
-  // counters [tile][rank][4]).
+  // (each half's partial of the other half's 128 columns in `partial` as
+  // [tile][half][128 columns][256 rows], row fastest; flags [tile][half][rank][4]).
   int tail_first;
   int num_items;
+  int debug_drop;       // test hook: the second K halves never raise their flags
   // CTA-pair kernel, many waves: items after each pair's first are claimed from
   // this counter (zero at launch); null: the static order
   int* tile_ctr;
@@ -87,10 +88,10 @@ constexpr int kSplitKMinSlabs = 48;
 // Sum of the split-K partials of launch L in chunk order, epilogue, one rounding (after launch_plain).
 cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream);
 // CTA-pair variant: 256 x 256 tiles per cluster of two; tensor maps use 128-row boxes for A and B.
-// Its tail split needs at least this many 64-deep K slabs: the hand-off of the
-// halves (partials through L2, a counter, the later half's sum) costs a few
+// Its tail split needs at least this many 64-deep K slabs: the exchange between
+// the halves (a partial of 128 columns each way through L2, flags) costs a few
 // microseconds, which only long enough tiles win back.
-constexpr int kTailSplitMinSlabs = 96;
+constexpr int kTailSplitMinSlabs = 48;
 // From this many waves of items on, the pair kernel claims items dynamically
 // (DRAM re-reads of the static order grow with the drift between pairs).
 constexpr int kPairClaimMinWaves = 16;

@@ -220,32 +220,6 @@ static_assert(L2ProgramCheck{}.ok, "the L2-accumulating programs must compute C_
 __constant__ StepOps d_l2_programs[kItemTypes][kSteps1] = LCG_L2_PROGRAMS;
 __constant__ int d_item_steps[kItemTypes] = {7, 4, 3, 7};
 
-__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Bounded wait for a split Group's partner: *flag >= target, else kErrFixupTimeout.
-__device__ __forceinline__ bool wait_flag(const int* flag, int target, const WaitCtl& w) {
-  if (ld_acquire_gpu(flag) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (ld_acquire_gpu(flag) >= target) return true;
-    if ((i & 31u) == 0) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.timeout_ns) {
-        record_error(w, kErrFixupTimeout);
-        return false;
-      }
-    }
-  }
-}
-
 // Work item w of this launch -> Group index and item type.
 // With Group ordering on, every pair walks its whole Groups in one product
 // order, so the pairs of a wave stream one product's operand panels at a time;

@@ -96,6 +96,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// ---------------------------------------------------------------- flags between CTAs
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for a split work item's partner: *flag >= target, else kErrFixupTimeout.
+__device__ __forceinline__ bool wait_flag(const int* flag, int target, const WaitCtl& w) {
+  if (ld_acquire_gpu(flag) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    if ((i & 31u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        record_error(w, kErrFixupTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 //
 // A kernel launched with programmatic stream serialisation may start while the

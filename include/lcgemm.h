@@ -113,8 +113,9 @@ enum {
   LCGEMM_OPT_MAX_CTAS = 4,         /* cap on the persistent grid (default 0 = one CTA per SM)         */
   LCGEMM_OPT_PEAK_GFLOPS = 5,      /* cost model: dense FP16/BF16 tensor peak, GFLOP/s                */
   LCGEMM_OPT_HBM_GBPS = 6,         /* cost model: HBM bandwidth, GB/s                                 */
-  LCGEMM_OPT_DEBUG_DROP_SIGNAL = 7, /* test hook: a split Group's partner never signals, so the
-                                      owner's bounded wait runs out (no fault, no hang)               */
+  LCGEMM_OPT_DEBUG_DROP_SIGNAL = 7, /* test hook: a split Group's partner (Strassen) or a split tail
+                                      tile's second K half (plain CTA-pair kernel) never signals, so
+                                      the waiting side's bounded wait runs out (no fault, no hang)   */
   LCGEMM_OPT_PLAIN_KERNEL = 8,      /* plain GEMM kernel: 0 choose (default: the GEMV for M <= 2; CTA
                                       pairs when M, N > 128 and their 256x256 tiles fill a quarter of
                                       the pairs; else single-CTA tiles with split-K), 1 single-CTA

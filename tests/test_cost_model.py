@@ -67,13 +67,19 @@ def test_wave_quantisation():
     h.close()
 
 
-def test_tail_split_from_96_slabs(plan):
-    """The partial last wave runs as K halves from 96 K slabs (K = 6144): 80 tiles then cost about
-    one and a half waves; with 64 slabs (K = 4096) the hand-off does not pay and they cost two."""
-    def ratio(K):
-        return plan.estimate(1024, 256 * 20, K, lcg.BF16, "plain") / plan.estimate(1024, 256 * 19, K, lcg.BF16, "plain")
-    assert ratio(6144) < 1.7
-    assert ratio(4096) > 1.7
+def test_tail_split_from_48_slabs(plan):
+    """The partial last wave runs as K halves from 48 K slabs (K = 3072): 80 tiles then cost about
+    one and a half waves of 76; with 32 slabs (K = 2048) the exchange does not pay, and the model
+    prices 80 tiles as with the split switched off."""
+    nosplit = lcg.Handle(lcg.PLANNING_DEVICE)
+    nosplit.set_option(lcg.OPT_SPLIT, 0)
+
+    def ratio(h, K):
+        return h.estimate(1024, 256 * 20, K, lcg.BF16, "plain") / h.estimate(1024, 256 * 19, K, lcg.BF16, "plain")
+    for K in (3072, 4096, 6144):
+        assert ratio(plan, K) < 1.7 < ratio(nosplit, K)
+    assert ratio(plan, 2048) == pytest.approx(ratio(nosplit, 2048))
+    nosplit.close()
 
 
 def test_strassen_saves_multiplies_only_when_large(plan):

@@ -329,3 +329,26 @@ def test_claimed_items_with_epilogue():
     assert h.sync_status() == 0
     assert torch.equal(C, C2)
     h.close()
+
+
+def test_tail_split_partner_timeout_is_reported_and_recovered():
+    """Failure detection without a GPU fault: the second K halves of the split tail tiles never
+    raise their flags, so the first halves' bounded waits run out; the kernel ends, the next status
+    call reports LCGEMM_ERR_TIMEOUT once, and the handle keeps working (same shape, exact again)."""
+    h = lcg.Handle(0)
+    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    h.set_option(lcg.OPT_WAIT_TIMEOUT_US, 50000)
+    M, N, K = 4096, 4096, 8192                   # 256 tiles: 3 waves of 76 pairs + 28 split tiles
+    A, B = synthetic.operands(M, N, K, "int3", 23, "bf16", "cuda")
+    h.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 1)
+    h.run(A, B, algo="plain")
+    torch.cuda.synchronize()
+    assert h.sync_status() == lcg.ERR_TIMEOUT
+    assert h.sync_status() == lcg.OK
+    h.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 0)
+    C = h.run(A, B, algo="plain")
+    torch.cuda.synchronize()
+    assert h.sync_status() == lcg.OK
+    rows = synthetic.row_sample(M, 256)
+    assert_bit_exact(C, oracle_c64(A, B, "bf16", rows=rows), "bf16", rows=rows)
+    h.close()
