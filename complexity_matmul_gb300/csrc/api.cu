@@ -173,25 +173,41 @@ int grid_cap(const lcgemm_ctx* h) {
   return h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms;
 }
 
-// Single-CTA 128 x 256 tiles, CTA-pair 256 x 256 tiles (gemm_pair.cu) or the
-// weight-streaming skinny kernel (gemm_skinny.cu).
+double pair_waves(int64_t M, int64_t N, int64_t K, int bn, int pairs, bool split) {
+  if (pairs <= 0) return 0.0;
+  const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+  const bool claimed = tiles >= int64_t(kPairClaimMinWaves) * pairs;
+  const int64_t full = tiles / pairs, rem = tiles - full * pairs;
+  double waves = static_cast<double>(full);
+  if (rem > 0)
+    waves += (split && !claimed && 2 * rem <= pairs && (K + kPlainBK - 1) / kPlainBK >= kTailSplitMinSlabs) ? 0.5 : 1.0;
+  return waves * (bn / 256);
+}
+
+int pair_tile_bn(int64_t M, int64_t N, int64_t K, int pairs, bool split) {
+  return pair_waves(M, N, K, 512, pairs, split) < kWideTileGain * pair_waves(M, N, K, 256, pairs, split) ? 512 : 256;
+}
+
+// Single-CTA 128 x 256 tiles (1), CTA-pair 256 x 256 (2) or 256 x 512 (5) tiles
+// (gemm_pair.cu), the weight-streaming skinny kernel (3, gemm_skinny.cu) or the GEMV (4).
 int plain_variant(const lcgemm_ctx* h, int64_t M, int64_t N, int64_t K) {
   const bool skinny_ok = M <= kSkinnyMaxM && (N + 127) / 128 <= (int64_t(1) << 20);
   if (h->plain_kernel == 4 && M <= kGemvMaxM) return 4;
   if (h->plain_kernel == 3 && skinny_ok) return 3;
   if (h->plain_kernel == 1) return 1;
   if (h->plain_kernel == 2) return grid_cap(h) < 2 ? 1 : 2;
+  if (h->plain_kernel == 5) return grid_cap(h) < 2 ? 1 : 5;
   // measured choices: one or two rows stream B best on the CUDA cores (at four
   // the FMA work makes the tiled split-K kernel faster); CTA pairs once their
   // 256 x 256 tiles fill a quarter of the pairs' slots; otherwise the single-CTA
   // tiles, whose split-K spreads a few tiles over the machine.  (The stream-K
   // skinny kernel measured at best level with split-K since the latter's deep
   // splits are summed by a separate kernel; it stays available as an option.)
-  (void)K;
   if (M <= 2) return 4;
   if (grid_cap(h) < 2) return 1;
   const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-  return (M > 128 && N > 128 && pair_tiles >= grid_cap(h) / 4) ? 2 : 1;
+  if (!(M > 128 && N > 128 && pair_tiles >= grid_cap(h) / 4)) return 1;
+  return pair_tile_bn(M, N, K, grid_cap(h) / 2, h->split != 0) == 512 ? 5 : 2;
 }
 
 // Tile width of the single-CTA kernel: 256 columns, 128 for narrow C, and 96
@@ -299,13 +315,13 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   PlainLaunch L{};
   L.bf16 = bf16;
   L.pdl = h->pdl != 0;
-  const bool pair = variant == 2;
+  const bool pair = variant == 2 || variant == 5;
   const int bm = pair ? 2 * kPlainBM : kPlainBM;
-  L.bn = pair ? 256 : plain_single_bn(M, N, grid_cap(h));
+  L.bn = variant == 5 ? 512 : pair ? 256 : plain_single_bn(M, N, grid_cap(h));
   // one tile row: the A box covers only the rows that exist (a multiple of 8)
   const int a_rows = (!pair && M < kPlainBM) ? static_cast<int>((M + 7) / 8 * 8) : kPlainBM;
   if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, a_rows)) return LCGEMM_ERR_CUDA;
-  if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, pair ? L.bn / 2 : L.bn)) return LCGEMM_ERR_CUDA;
+  if (!encode_kmajor(&L.tmB, bf16, B, N, K, ldb, pair ? 128 : L.bn)) return LCGEMM_ERR_CUDA;
   PlainArgs& a = L.args;
   a.C = C;
   a.ldc = ldc;
@@ -375,7 +391,7 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     a.num_items = split ? full * P + 2 * rem : a.num_tiles;
     a.debug_drop = h->debug_drop;
     if (split) {
-      const size_t part_bytes = static_cast<size_t>(rem) * 2 * 256 * 128 * sizeof(float);
+      const size_t part_bytes = static_cast<size_t>(rem) * 2 * 256 * (L.bn / 2) * sizeof(float);
       const size_t off = (part_bytes + 255) / 256 * 256;
       const size_t ctr_bytes = static_cast<size_t>(rem) * 2 * 2 * 4 * sizeof(int);
       int rc = ensure_workspace(h, off + ctr_bytes, st);
@@ -731,7 +747,7 @@ int lcgemm_set_option(lcgemm_t h, int option, int64_t value) {
       h->debug_drop = static_cast<int>(value);
       return LCGEMM_OK;
     case LCGEMM_OPT_PLAIN_KERNEL:
-      if (value < 0 || value > 4) return LCGEMM_ERR_ARG;
+      if (value < 0 || value > 5) return LCGEMM_ERR_ARG;
       h->plain_kernel = static_cast<int>(value);
       return LCGEMM_OK;
     case LCGEMM_OPT_PDL:

@@ -1,4 +1,4 @@
-// Plain GEMM on CTA pairs (cta_group::2): 256 x 256 output tiles per pair.
+// Plain GEMM on CTA pairs (cta_group::2): 256 x 256 or 256 x 512 output tiles per pair.
 //
 // Same pipeline as the single-CTA kernel (TMA producer, MMA issuer, four
 // epilogue warps, two TMEM accumulators), but each tcgen05.mma covers M = 256
@@ -50,21 +50,37 @@ namespace lcg {
 namespace {
 
 constexpr int kBM = 128;           // rows per CTA (256 per pair)
-constexpr int kBN = 256;           // columns per pair (128 B rows staged per CTA)
 constexpr int kBK = 64;
-constexpr int kStages = 6;
 constexpr int kThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = (kBN / 2) * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kTxBytes = 2 * kStageBytes;
-constexpr int kTmemCols = 2 * kBN;
+constexpr int kBBox = 128 * kBK * 2;  // one 128-row B box: a CTA's share of one 256-column MMA
+constexpr int kTmemCols = 512;
+
+// Tile of 256 x (256 * NB) per pair: per 16-deep K step NB MMAs of N = 256 share
+// the A operand.  NB = 1: six 32 KB stages and two accumulators (the epilogue of
+// one tile overlaps the next tile's main loop).  NB = 2: four 48 KB stages and
+// one 512-column accumulator (the epilogue does not overlap), but each A slab
+// serves 512 columns: a quarter less operand traffic from L2 per flop.
+template <int NB>
+struct PairCfg {
+  static constexpr int kBN = 256 * NB;
+  static constexpr int kStages = NB == 1 ? 6 : 4;
+  static constexpr int kBBytes = NB * kBBox;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTxBytes = 2 * kStageBytes;
+  static constexpr int kAccs = NB == 1 ? 2 : 1;
+  static_assert(kAccs * kBN == kTmemCols, "accumulators fill tensor memory");
+};
 constexpr int kQ = 4;              // queue slots (DYN): items published but not yet read by every role
 constexpr int kQReaders = 10;      // the leader's MMA issuer, the partner's producer, 8 epilogue warps
 constexpr int kClaimLead = 8;      // the next item is claimed this many slabs before the current one ends
 constexpr int kCBoxBytes = 32 * 32 * 2;            // one epilogue warp's 32 x 32 chunk of C
 constexpr int kCStageBytes = 4 * 2 * kCBoxBytes;     // two boxes per epilogue warp
-constexpr int kSmemBytes = kStages * kStageBytes + kCStageBytes + 512 + 1024;
+template <int NB>
+constexpr int pair_smem_bytes() {
+  return PairCfg<NB>::kStages * PairCfg<NB>::kStageBytes + kCStageBytes + 512 + 1024;
+}
+static_assert(pair_smem_bytes<1>() <= 232448 && pair_smem_bytes<2>() <= 232448, "shared memory budget");
 
 // Cast of one 32 x 32 chunk (lane = row, v = its 32 columns) into a shared-memory
 // box of 32 rows x 64 bytes laid out in the tensor map's 64-byte swizzle: 16-byte
@@ -154,10 +170,12 @@ __device__ __forceinline__ void emit_chunk(float (&v)[32], int row, int row0, in
   }
 }
 
-template <bool BF16, bool EPI, bool DYN>
+template <bool BF16, bool EPI, bool DYN, int NB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     plain_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const PlainArgs args) {
+  using Cfg = PairCfg<NB>;
+  constexpr int kBN = Cfg::kBN, kStages = Cfg::kStages, kBBytes = Cfg::kBBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem;
@@ -246,10 +264,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[stage], kTxBytes);
+          if (leader) mbar_arrive_expect_tx(&full[stage], Cfg::kTxBytes);
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           tma_load_2d_pair(sA + stage * kABytes, &tmA, bar, kb * kBK, mb * 2 * kBM + rank * kBM);
-          tma_load_2d_pair(sB + stage * kBBytes, &tmB, bar, kb * kBK, nb * kBN + rank * (kBN / 2));
+          // B: for each 256-column part of the tile, this CTA's 128 rows
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            tma_load_2d_pair(sB + stage * kBBytes + j * kBBox, &tmB, bar, kb * kBK, nb * kBN + j * 256 + rank * 128);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -272,7 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_f16(BF16, 2 * kBM, kBN);
+      constexpr uint32_t idesc = idesc_f16(BF16, 2 * kBM, 256);
       // descriptors of stage 0; a stage / K-step offset is added to the start-address field
       const uint64_t a_desc0 = sdesc_k128(smem_u32(sA));
       const uint64_t b_desc0 = sdesc_k128(smem_u32(sB));
@@ -290,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kBN;
+        const uint32_t d_tmem = tmem_base + acc * kBN;   // NB parts of 256 columns
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, wc)) {
             ok = false;
@@ -301,7 +322,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+              mma_f16_pair(d_tmem + j * 256, ad + 2 * k, bd + ((j * kBBox) >> 4) + 2 * k, idesc,
+                           (kb != kb0 || k != 0) ? 1u : 0u);
           mma_commit_pair(&empty[stage]);
           issued = true;
           if (++stage == kStages) {
@@ -311,8 +335,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit_pair(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == Cfg::kAccs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
       if (!ok && issued) {
         mma_commit_pair(drain);
@@ -429,8 +455,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (++acc == Cfg::kAccs) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
     }
     if (lane == 0) bulk_wait_all();   // the tensor stores have read their boxes and written C
   }
@@ -443,27 +471,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool BF16, bool EPI, bool DYN>
+template <bool BF16, bool EPI, bool DYN, int NB>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
-  auto kern = plain_pair_kernel<BF16, EPI, DYN>;
+  auto kern = plain_pair_kernel<BF16, EPI, DYN, NB>;
+  constexpr int smem = pair_smem_bytes<NB>();
   {
-    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes);
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.tmC, L.args);
+  return launch_maybe_pdl(kern, L.grid, kThreads, smem, stream, L.pdl, L.tmA, L.tmB, L.tmC, L.args);
+}
+
+}  // namespace
+
+namespace {
+
+template <int NB>
+cudaError_t launch_width(const PlainLaunch& L, cudaStream_t stream) {
+  // the kernel without an epilogue keeps the lean store path
+  if (L.args.tile_ctr) {
+    if (L.args.ep.on)
+      return L.bf16 ? launch_impl<true, true, true, NB>(L, stream) : launch_impl<false, true, true, NB>(L, stream);
+    return L.bf16 ? launch_impl<true, false, true, NB>(L, stream) : launch_impl<false, false, true, NB>(L, stream);
+  }
+  if (L.args.ep.on)
+    return L.bf16 ? launch_impl<true, true, false, NB>(L, stream) : launch_impl<false, true, false, NB>(L, stream);
+  return L.bf16 ? launch_impl<true, false, false, NB>(L, stream) : launch_impl<false, false, false, NB>(L, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream) {
   if (L.grid % 2) return cudaErrorInvalidValue;
-  // the kernel without an epilogue keeps the lean store path
-  if (L.args.tile_ctr) {
-    if (L.args.ep.on) return L.bf16 ? launch_impl<true, true, true>(L, stream) : launch_impl<false, true, true>(L, stream);
-    return L.bf16 ? launch_impl<true, false, true>(L, stream) : launch_impl<false, false, true>(L, stream);
-  }
-  if (L.args.ep.on) return L.bf16 ? launch_impl<true, true, false>(L, stream) : launch_impl<false, true, false>(L, stream);
-  return L.bf16 ? launch_impl<true, false, false>(L, stream) : launch_impl<false, false, false>(L, stream);
+  if (L.bn == 512) return launch_width<2>(L, stream);
+  if (L.bn == 256) return launch_width<1>(L, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace lcg

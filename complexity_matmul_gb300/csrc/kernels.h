@@ -68,7 +68,7 @@ struct PlainLaunch {
   CUtensorMap tmA, tmB;
   CUtensorMap tmC;      // CTA-pair kernel: C in 32 x 32 boxes, 64-byte swizzle (tensor stores)
   PlainArgs args;
-  int bn;               // 128 or 256
+  int bn;               // single-CTA kernel: 96, 128 or 256; CTA-pair kernel: 256 or 512
   bool bf16;
   int grid;
   bool pdl;             // launch as a programmatic dependent of the kernel before it
@@ -95,6 +95,11 @@ constexpr int kTailSplitMinSlabs = 48;
 // From this many waves of items on, the pair kernel claims items dynamically
 // (DRAM re-reads of the static order grow with the drift between pairs).
 constexpr int kPairClaimMinWaves = 16;
+// Per unit of work, 256 x 512 pair tiles (two 256-column MMAs sharing each A
+// slab) ran ~5 % faster than 256 x 256 ones at 8192^3 (quarter less operand
+// traffic from L2; under the power cap ~6 % at 16384^3); they are chosen when
+// their wave-quantised time divided by this is below the narrow tiles'.
+constexpr double kWideTileGain = 1.05;
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 
 // Skinny GEMM (M <= 256): C^T = B . A^T with 128-row blocks of B as the MMA's

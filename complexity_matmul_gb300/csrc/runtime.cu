@@ -93,17 +93,17 @@ double estimate_seconds(const lcgemm_ctx* h, int algo, int64_t M, int64_t N, int
   if (algo == LCGEMM_PLAIN) {
     const double bytes = 2.0 * (m * k + k * n + m * n);
     const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
-    const bool pair = sms >= 2 && (h->plain_kernel == 2 ||
+    const bool pair = sms >= 2 && (h->plain_kernel == 2 || h->plain_kernel == 5 ||
                                    (h->plain_kernel == 0 && M > 128 && N > 128 && pair_tiles >= sms / 4));
     if (pair) {
-      // the partial last wave runs as K halves when it fits twice over
-      const int64_t tiles = cdiv(M, 256) * cdiv(N, 256);
+      // waves of 256 x 256 or 256 x 512 tiles (the dispatcher's width), the partial
+      // last wave as K halves when it is split; wide tiles do more per unit of time
       const int units = sms / 2;
-      const int64_t full = tiles / units, rem = tiles - full * units;
-      double eff = wave_efficiency(tiles, units);
-      if (h->split && rem > 0 && 2 * rem <= units && cdiv(K, 64) >= kTailSplitMinSlabs)
-        eff = static_cast<double>(tiles) / ((static_cast<double>(full) + 0.5) * units);
-      return std::max(mnk2 / (kEtaPlainPair * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
+      const int bn = h->plain_kernel == 2 ? 256 : h->plain_kernel == 5 ? 512
+                                                 : pair_tile_bn(M, N, K, units, h->split != 0);
+      const double eff = static_cast<double>(pair_tiles) / (units * pair_waves(M, N, K, bn, units, h->split != 0));
+      const double eta = kEtaPlainPair * (bn == 512 ? kWideTileGain : 1.0);
+      return std::max(mnk2 / (eta * P * eff), bytes / (kBetaStream * BW)) + kLaunchSec;
     }
     // single-CTA tiles with the launcher's split-K: tiles x chunks work items, FP32
     // partials written and read back, deep splits summed by a separate kernel

@@ -98,7 +98,7 @@ def test_epilogue_entry_rejects_planning_and_null_handles(library):
 @pytest.mark.parametrize("option,bad", [(lcg.OPT_WAIT_TIMEOUT_US, 0), (lcg.OPT_WAIT_TIMEOUT_US, 61_000_000),
                                         (lcg.OPT_GROUP_ORDER, 2), (lcg.OPT_SPLIT, -1), (lcg.OPT_MAX_CTAS, -1),
                                         (lcg.OPT_PEAK_GFLOPS, 0), (lcg.OPT_HBM_GBPS, -5),
-                                        (lcg.OPT_DEBUG_DROP_SIGNAL, 3), (lcg.OPT_PLAIN_KERNEL, 5),
+                                        (lcg.OPT_DEBUG_DROP_SIGNAL, 3), (lcg.OPT_PLAIN_KERNEL, 6),
                                         (lcg.OPT_LCMA_KERNEL, 3), (lcg.OPT_PDL, 2), (999, 1)])
 def test_set_option_rejects_bad_values(option, bad):
     """Every option checks its range (and unknown keys are refused) with LCGEMM_ERR_ARG, on a

@@ -71,15 +71,35 @@ def test_tail_split_from_48_slabs(plan):
     """The partial last wave runs as K halves from 48 K slabs (K = 3072): 80 tiles then cost about
     one and a half waves of 76; with 32 slabs (K = 2048) the exchange does not pay, and the model
     prices 80 tiles as with the split switched off."""
-    nosplit = lcg.Handle(lcg.PLANNING_DEVICE)
+    split, nosplit = lcg.Handle(lcg.PLANNING_DEVICE), lcg.Handle(lcg.PLANNING_DEVICE)
+    for h in (split, nosplit):
+        h.set_option(lcg.OPT_PLAIN_KERNEL, 2)        # 256 x 256 pair tiles
     nosplit.set_option(lcg.OPT_SPLIT, 0)
 
     def ratio(h, K):
         return h.estimate(1024, 256 * 20, K, lcg.BF16, "plain") / h.estimate(1024, 256 * 19, K, lcg.BF16, "plain")
     for K in (3072, 4096, 6144):
-        assert ratio(plan, K) < 1.7 < ratio(nosplit, K)
-    assert ratio(plan, 2048) == pytest.approx(ratio(nosplit, 2048))
+        assert ratio(split, K) < 1.7 < ratio(nosplit, K)
+    assert ratio(split, 2048) == pytest.approx(ratio(nosplit, 2048))
+    split.close()
     nosplit.close()
+
+
+def test_pair_tile_width():
+    """256 x 512 pair tiles when their wave-quantised time, less the wide tiles' measured ~5 % per
+    unit of work, beats 256 x 256 tiles: 16384^3 (27 waves against 54) and 8192^3 (7 waves of
+    double length against 13.5 with the tail split) take them; 4096^3 (2 against 3.5) and 2048^3
+    (one wave either way: twice as long) do not.  The model prices whichever the dispatcher takes."""
+    wide, narrow, auto = (lcg.Handle(lcg.PLANNING_DEVICE) for _ in range(3))
+    wide.set_option(lcg.OPT_PLAIN_KERNEL, 5)
+    narrow.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    for n, want in ((16384, wide), (8192, wide), (4096, narrow), (2048, narrow)):
+        t = auto.estimate(n, n, n, lcg.BF16, "plain")
+        assert t == pytest.approx(want.estimate(n, n, n, lcg.BF16, "plain"))
+        other = narrow if want is wide else wide
+        assert t < other.estimate(n, n, n, lcg.BF16, "plain")
+    for h in (wide, narrow, auto):
+        h.close()
 
 
 def test_strassen_saves_multiplies_only_when_large(plan):
@@ -175,12 +195,15 @@ def test_h20_like_machine_picks_strassen_only_for_large_cubes():
     A Strassen efficiency that cannot reach 7/8 of plain's never picks it (first assertion);
     a model without the refill cost picks it at 8192^3 too (second)."""
     h = _h20_like()
-    for n in (12288, 16384):
+    for n in (16384, 20480):
         assert h.select(n, n, n, lcg.BF16) in (lcg.STRASSEN1, lcg.STRASSEN2), n
     # a second level pays once the cube is large enough to amortise its larger pre-pass
     assert h.select(24576, 24576, 24576, lcg.BF16) == lcg.STRASSEN2
     for n in (2048, 4096, 8192):
         assert h.select(n, n, n, lcg.BF16) == lcg.PLAIN, n
+    # 12288^3 sits at the crossover (plain's 256 x 512 tiles within 2 % of one level)
+    t = {a: h.estimate(12288, 12288, 12288, lcg.BF16, a) for a in ("plain", "strassen1")}
+    assert abs(t["plain"] / t["strassen1"] - 1) < 0.05
     h.close()
 
 

@@ -15,7 +15,7 @@ from helpers import (MAXERR_SIGMA, assert_bit_exact, assert_epilogue_close, orac
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2, 3, 4], ids=["single_cta", "cta_pair", "skinny", "gemv"])
+@pytest.fixture(scope="module", params=[1, 2, 3, 4, 5], ids=["single_cta", "cta_pair", "skinny", "gemv", "cta_pair_512"])
 def h(request):
     """Plain tests run on each plain kernel (3: the skinny kernel where M <= 256, 4: the GEMV where
     M <= 4), Strassen tests on both fused one-level kernels."""

@@ -12,10 +12,11 @@ from helpers import assert_bit_exact, assert_close, assert_epilogue_close, oracl
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2, 3, 4], ids=["single_cta", "cta_pair", "skinny", "gemv"])
+@pytest.fixture(scope="module", params=[1, 2, 3, 4, 5], ids=["single_cta", "cta_pair", "skinny", "gemv", "cta_pair_512"])
 def h(request):
     """Every plain test runs on each kernel: single-CTA 128x256 tiles, CTA-pair 256x256 tiles, the
-    stream-K skinny kernel (M <= 256) and the CUDA-core GEMV (M <= 4); other M choose."""
+    stream-K skinny kernel (M <= 256), the CUDA-core GEMV (M <= 4; other M choose) and CTA-pair
+    256x512 tiles."""
     handle = lcg.Handle(0)
     handle.set_option(lcg.OPT_PLAIN_KERNEL, request.param)
     yield handle
