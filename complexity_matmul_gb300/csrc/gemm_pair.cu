@@ -1,12 +1,13 @@
 // Plain GEMM on CTA pairs (cta_group::2): 256 x 256 or 256 x 512 output tiles per pair.
 //
 // Same pipeline as the single-CTA kernel (TMA producer, MMA issuer, four
-// epilogue warps, two TMEM accumulators), but each tcgen05.mma covers M = 256
-// rows: the even CTA of a cluster of two issues it, each CTA stages 128 rows
-// of A and 128 of the 256 B rows in its own shared memory, and each CTA keeps
-// its 128 accumulator rows in its own tensor memory.  Per SM the tensor core
-// reads 16 KB of A and 8 KB of (its half of) B per 64-deep K slab instead of
-// 16 KB + 32 KB, which halves the shared-memory and L2 traffic per flop.
+// epilogue warps, accumulators in tensor memory), but each tcgen05.mma covers
+// M = 256 rows: the even CTA of a cluster of two issues it, each CTA stages 128
+// rows of A and its half of the tile's B rows in its own shared memory, and
+// each CTA keeps its 128 accumulator rows in its own tensor memory.  Per SM
+// and 256 x 256 x 64 step the tensor core reads 16 KB of A and 16 KB of B
+// instead of 16 KB + 32 KB, which halves the shared-memory and L2 traffic per
+// flop; 512-column tiles let two such steps share the A slab.
 //
 // Epilogue: each warp casts 32 x 32 chunks of its 32 accumulator rows into two
 // alternating shared-memory boxes and writes each with one tensor store, so C
