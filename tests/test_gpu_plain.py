@@ -282,28 +282,30 @@ def test_one_row_96_column_tiles(M, N, K):
 
 # ---------------------------------------------------------------- claimed items (CTA-pair kernel, many waves)
 
+@pytest.mark.parametrize("kernel", [2, 5], ids=["tiles256", "tiles512"])
 @pytest.mark.parametrize("ctas,M,N,K,dtype", [(8, 2048, 2048, 512, "bf16"), (8, 1900, 2100, 700, "f16"),
                                               (16, 2560, 3328, 6144, "bf16")])
-def test_claimed_items_bit_exact(ctas, M, N, K, dtype):
+def test_claimed_items_bit_exact(kernel, ctas, M, N, K, dtype):
     """With at least 16 waves of items the CTA-pair kernel claims every pair's later items from a
     counter.  A cap of 8 or 16 CTAs (4 or 8 pairs) puts small shapes there: exactly 16 waves, a
     ragged edge, and 130 tiles with the tail split (16 full waves + 2 tiles as K halves).  Integer
     inputs bit-exact against the oracle, the same bits as the static order on the full machine, and
-    stable over back-to-back launches (the counter starts from zero each time)."""
+    stable over back-to-back launches (the counter starts from zero each time).  On both tile widths;
+    the 256 x 512 tiles run on half the CTAs (2 or 4 pairs), so that the same shapes have 16 waves."""
     A, B = synthetic.operands(M, N, K, "int3", 81, dtype, "cuda")
     rows = None if M * N * K <= 4e9 else synthetic.row_sample(M, 256)
     ref = oracle_c64(A, B, dtype, rows=rows)
     A, B = padded(M, K, dtype, A), padded(N, K, dtype, B)   # 16-byte row starts for any K
     h = lcg.Handle(0)
-    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
-    h.set_option(lcg.OPT_MAX_CTAS, ctas)
+    h.set_option(lcg.OPT_PLAIN_KERNEL, kernel)
+    h.set_option(lcg.OPT_MAX_CTAS, ctas if kernel == 2 else ctas // 2)
     Cs = [h.run(A, B, algo="plain") for _ in range(4)]
     torch.cuda.synchronize()
     assert h.sync_status() == 0
     assert_bit_exact(Cs[0], ref, dtype, rows=rows)
     assert all(torch.equal(Cs[0], C) for C in Cs[1:])
     full = lcg.Handle(0)
-    full.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    full.set_option(lcg.OPT_PLAIN_KERNEL, kernel)
     assert torch.equal(_run(full, A, B), Cs[0])
     full.close()
     h.close()
@@ -332,14 +334,19 @@ def test_claimed_items_with_epilogue():
     h.close()
 
 
-def test_tail_split_partner_timeout_is_reported_and_recovered():
+@pytest.mark.parametrize("kernel", [2, 5], ids=["tiles256", "tiles512"])
+def test_tail_split_partner_timeout_is_reported_and_recovered(kernel):
     """Failure detection without a GPU fault: the second K halves of the split tail tiles never
     raise their flags, so the first halves' bounded waits run out; the kernel ends, the next status
     call reports LCGEMM_ERR_TIMEOUT once, and the handle keeps working (same shape, exact again)."""
     h = lcg.Handle(0)
-    h.set_option(lcg.OPT_PLAIN_KERNEL, 2)
+    h.set_option(lcg.OPT_PLAIN_KERNEL, kernel)
     h.set_option(lcg.OPT_WAIT_TIMEOUT_US, 50000)
-    M, N, K = 4096, 4096, 8192                   # 256 tiles: 3 waves of 76 pairs + 28 split tiles
+    # 256 x 256 tiles: 256 = 3 waves of 76 pairs + 28 split; 256 x 512 tiles: 128 = 1 wave of 76 + 52,
+    # which do not fit twice over, so 24 pairs (48 CTAs) run them: 5 waves + 8 split
+    M, N, K = 4096, 4096, 8192
+    if kernel == 5:
+        h.set_option(lcg.OPT_MAX_CTAS, 48)
     A, B = synthetic.operands(M, N, K, "int3", 23, "bf16", "cuda")
     h.set_option(lcg.OPT_DEBUG_DROP_SIGNAL, 1)
     h.run(A, B, algo="plain")
