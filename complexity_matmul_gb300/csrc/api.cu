@@ -176,12 +176,15 @@ int grid_cap(const lcgemm_ctx* h) {
 double pair_waves(int64_t M, int64_t N, int64_t K, int bn, int pairs, bool split) {
   if (pairs <= 0) return 0.0;
   const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+  const double kb = static_cast<double>((K + kPlainBK - 1) / kPlainBK);
   const bool claimed = tiles >= int64_t(kPairClaimMinWaves) * pairs;
   const int64_t full = tiles / pairs, rem = tiles - full * pairs;
-  double waves = static_cast<double>(full);
-  if (rem > 0)
-    waves += (split && !claimed && 2 * rem <= pairs && (K + kPlainBK - 1) / kPlainBK >= kTailSplitMinSlabs) ? 0.5 : 1.0;
-  return waves * (bn / 256);
+  const bool halves = rem > 0 && split && !claimed && 2 * rem <= pairs && kb >= kTailSplitMinSlabs;
+  const double waves = static_cast<double>(full) + (rem == 0 ? 0.0 : halves ? 0.5 : 1.0);
+  double t = waves * (bn / 256);
+  if (bn == 512) t += static_cast<double>(full + (rem > 0 ? 1 : 0)) * kWideEpilogueSlabs / kb;
+  if (halves) t += kSplitExchangeSlabs / kb;
+  return t;
 }
 
 int pair_tile_bn(int64_t M, int64_t N, int64_t K, int pairs, bool split) {

@@ -95,11 +95,16 @@ constexpr int kTailSplitMinSlabs = 48;
 // From this many waves of items on, the pair kernel claims items dynamically
 // (DRAM re-reads of the static order grow with the drift between pairs).
 constexpr int kPairClaimMinWaves = 16;
-// Per unit of work, 256 x 512 pair tiles (two 256-column MMAs sharing each A
-// slab) ran ~5 % faster than 256 x 256 ones at 8192^3 (quarter less operand
-// traffic from L2; under the power cap ~6 % at 16384^3); they are chosen when
-// their wave-quantised time divided by this is below the narrow tiles'.
+// Width of the pair tiles: 256 x 512 tiles (two 256-column MMAs sharing each A
+// slab; a quarter less operand traffic from L2) do ~5 % more work per unit of
+// time than 256 x 256 ones in long main loops (under the power cap ~6 % at
+// 16384^3), but their one accumulator keeps each tile's epilogue out of the next
+// tile's main loop (~3 us, about 10 slabs of a 256 x 256 tile), and a split tail
+// costs an exchange of about as much.  The dispatcher compares the two widths'
+// wave-quantised times with these terms.
 constexpr double kWideTileGain = 1.05;
+constexpr double kWideEpilogueSlabs = 10.0;
+constexpr double kSplitExchangeSlabs = 10.0;
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);
 
 // Skinny GEMM (M <= 256): C^T = B . A^T with 128-row blocks of B as the MMA's

@@ -49,7 +49,8 @@ int grid_cap(const lcgemm_ctx* h);
 int plain_single_bn(int64_t M, int64_t N, int sms);
 // CTA-pair tiles of 256 x bn (bn = 256 or 512) on `pairs` pairs: the launch's time
 // in units of one 256 x 256 tile's main loop (full waves, the partial last wave as
-// K halves when the launcher splits it, each wave bn / 256 units long).
+// K halves when the launcher splits it, each wave bn / 256 units long, plus the
+// wide tiles' epilogues and the split tail's exchange).
 double pair_waves(int64_t M, int64_t N, int64_t K, int bn, int pairs, bool split);
 // The width the dispatcher takes for CTA-pair tiles (256 or 512).
 int pair_tile_bn(int64_t M, int64_t N, int64_t K, int pairs, bool split);

@@ -86,18 +86,22 @@ def test_tail_split_from_48_slabs(plan):
 
 
 def test_pair_tile_width():
-    """256 x 512 pair tiles when their wave-quantised time, less the wide tiles' measured ~5 % per
-    unit of work, beats 256 x 256 tiles: 16384^3 (27 waves against 54) and 8192^3 (7 waves of
-    double length against 13.5 with the tail split) take them; 4096^3 (2 against 3.5) and 2048^3
-    (one wave either way: twice as long) do not.  The model prices whichever the dispatcher takes."""
+    """256 x 512 pair tiles when their wave-quantised time, with ~10 slabs of epilogue per wide tile
+    and less their measured ~5 % per unit of work, beats 256 x 256 tiles: the long main loops of
+    16384^3 (27 waves against 54) and 12288^3 take them; the shapes where they measured slower do
+    not: K = 4096 (1024x14336, 4096x16384: 3-8 % slower), a split wide tail against one narrow
+    wave (1024x4096x14336), 4096^3 and 2048^3.  The model prices whichever the dispatcher takes."""
     wide, narrow, auto = (lcg.Handle(lcg.PLANNING_DEVICE) for _ in range(3))
     wide.set_option(lcg.OPT_PLAIN_KERNEL, 5)
     narrow.set_option(lcg.OPT_PLAIN_KERNEL, 2)
-    for n, want in ((16384, wide), (8192, wide), (4096, narrow), (2048, narrow)):
-        t = auto.estimate(n, n, n, lcg.BF16, "plain")
-        assert t == pytest.approx(want.estimate(n, n, n, lcg.BF16, "plain"))
+    cases = [((16384, 16384, 16384), wide), ((12288, 12288, 12288), wide),
+             ((1024, 14336, 4096), narrow), ((4096, 16384, 4096), narrow), ((1024, 4096, 14336), narrow),
+             ((4096, 4096, 4096), narrow), ((2048, 2048, 2048), narrow)]
+    for (m, n, k), want in cases:
+        t = auto.estimate(m, n, k, lcg.BF16, "plain")
+        assert t == pytest.approx(want.estimate(m, n, k, lcg.BF16, "plain")), (m, n, k)
         other = narrow if want is wide else wide
-        assert t < other.estimate(n, n, n, lcg.BF16, "plain")
+        assert t < other.estimate(m, n, k, lcg.BF16, "plain"), (m, n, k)
     for h in (wide, narrow, auto):
         h.close()
 
