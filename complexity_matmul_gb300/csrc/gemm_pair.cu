@@ -16,10 +16,10 @@
 //
 // Tail split (static order only): when the tiles of the partial last wave fit
 // twice over into the pairs, each runs as two K halves on two pairs.  Each half
-// publishes the FP32 partial of the 128 columns the other half finishes, raises
-// its flag, waits (bounded) for the other's flag, and finishes its own 128
-// columns as (0 + half 0) + half 1 from its accumulator and the other's
-// partial.  A pair has at most one such item, its last, and publishes before it
+// publishes the FP32 partial of the half of the tile's columns that the other
+// half finishes, raises its flag, waits (bounded) for the other's flag, and
+// finishes its own columns as (0 + half 0) + half 1 from its accumulator and
+// the other's partial.  A pair has at most one such item, its last, and publishes before it
 // waits, so the two halves cannot wait on each other in a cycle.
 //
 // Work distribution.  Few waves: pair p runs items p, p + P, p + 2P, ... (P
@@ -217,6 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -393,9 +394,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           emit_chunk<BF16, EPI>(v, row, row0, col, sbox + ((nbox++ & 1u) * kCBoxBytes), lane, &tmC, args, &cur);
         }
       } else {
-        // tail tile, K half `half`: the partial of the other half's 128 columns goes
-        // out (column-major per half: one cache line per warp store), then this
-        // half's 128 columns are finished from its accumulator and the other's partial
+        // tail tile, K half `half`: the partial of the columns the other half finishes
+        // goes out (column-major per half: one cache line per warp store), then this
+        // half's columns are finished from its accumulator and the other's partial
         const int i = tile - args.tail_first;
         const int slot_rows = 2 * kBM;
         const int64_t slot = int64_t(slot_rows) * (kBN / 2);
