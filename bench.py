@@ -8,11 +8,13 @@ the library's cost model (``LCGEMM_AUTO``).  ``value`` is sum(2 n^3) over the
 sweep divided by the summed device time of the four GEMMs (CUDA events on the
 launching stream, L2 flushed by a 256 MB write before every timed launch,
 outside the event pair).  Offline timing is per shape: each size gets its W
-warm-up launches and then its K timed launches back to back, sizes ascending.  ``server`` repeats the launches with seeded random
-0-5 ms host sleeps in between (the randomly spaced launch mode), ``e2e``
-times the host-buffer entry point ``lcgemm_run_host`` with page-locked inputs
-(host->device copies, the GEMM and the device->host copy of C inside the
-timed region).
+warm-up launches and then its K timed launches back to back, sizes ascending.
+``server`` repeats the launches with seeded random 0-5 ms host sleeps in
+between (the randomly spaced launch mode), ``e2e`` times the host-buffer entry
+point ``lcgemm_run_host`` with page-locked inputs (host->device copies, the
+GEMM and the device->host copy of C inside the timed region), and ``context``
+times torch.mm (cuBLAS) on the same operands the same way, as a labelled
+context line outside the library's timed region (``--no-cublas`` skips it).
 
 ``--impl reference`` times the CPU oracle (FP64 triple loop, OpenMP) on a
 bounded row sample of the same workload instead.
@@ -42,6 +44,7 @@ WORKLOAD = ("bf16 square sweep M=N=K in {2048,4096,8192,16384}; A row-major, B c
 METRIC = "effective TFLOPS (2MNK/t) FP16/BF16 GEMM, % of GB300 dense peak, offline+server"
 UNIT = "TFLOPS"
 L2_FLUSH_BYTES = 256 << 20
+CUBLAS_REPS = 5      # torch.mm context launches per size (not the library)
 
 
 def _dist():
@@ -258,6 +261,31 @@ def run_gpu(args):
                                 "tflops": round(2.0 * n ** 3 / (statistics.median(srv[n]) * 1e-3) / 1e12, 1)}
                        for n in SIZES}
 
+    # ---- context only (not on the library's path): cuBLAS through torch.mm on the same operands,
+    # timed with the same flush, device-side wait and events, a few launches per size
+    context = None
+    if not args.no_cublas:
+        ctx = {}
+        for n in SIZES:
+            A, B, C = ops[n]
+            for _ in range(2):
+                torch.mm(A, B.t(), out=C)
+            ts = []
+            for _ in range(CUBLAS_REPS):
+                flush.fill_(1.0)
+                torch.cuda._sleep(HOST_COVER_CYCLES)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                torch.mm(A, B.t(), out=C)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            med = statistics.median(ts)
+            ctx[str(n)] = {"median_ms": round(med, 4), "tflops": round(2.0 * n ** 3 / (med * 1e-3) / 1e12, 1)}
+        context = {"torch_mm_cublas": ctx, "reps": CUBLAS_REPS,
+                   "note": "context line, not the library: torch.mm (cuBLAS) on the same BF16 operands, "
+                           "single launches after the same L2 flush and device-side wait, CUDA events"}
+
     # ---- roofline of the dominant kernel (largest share of the step)
     peak_burst, peak_sust, hbm, peak_kind = _peaks()
     dom = max(SIZES, key=lambda n: statistics.median(per_n_ms[n]))
@@ -311,6 +339,8 @@ def run_gpu(args):
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
+        if context is not None:
+            line["context"] = context
         print(json.dumps(line), flush=True)
     h.close()
     if world > 1:
@@ -811,6 +841,7 @@ def main():
     ap.add_argument("--impl", choices=["lcgemm", "reference"], default="lcgemm")
     ap.add_argument("--server-reps", type=int, default=50)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the torch.mm (cuBLAS) context line")
     ap.add_argument("--case", default=None, help="profiling mode: run one shape 'n' or 'M,N,K' --reps times")
     ap.add_argument("--algo", default="auto", help="algorithm for --case")
     ap.add_argument("--reps", type=int, default=3, help="launches for --case")
