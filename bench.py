@@ -13,8 +13,9 @@ warm-up launches and then its K timed launches back to back, sizes ascending.
 between (the randomly spaced launch mode), ``e2e`` times the host-buffer entry
 point ``lcgemm_run_host`` with page-locked inputs (host->device copies, the
 GEMM and the device->host copy of C inside the timed region), and ``context``
-times torch.mm (cuBLAS) on the same operands the same way, as a labelled
-context line outside the library's timed region (``--no-cublas`` skips it).
+times torch.mm (cuBLAS) on the same operands with the offline protocol, as a
+labelled context line outside the library's timed region (``--no-cublas``
+skips it).
 
 ``--impl reference`` times the CPU oracle (FP64 triple loop, OpenMP) on a
 bounded row sample of the same workload instead.
@@ -44,7 +45,6 @@ WORKLOAD = ("bf16 square sweep M=N=K in {2048,4096,8192,16384}; A row-major, B c
 METRIC = "effective TFLOPS (2MNK/t) FP16/BF16 GEMM, % of GB300 dense peak, offline+server"
 UNIT = "TFLOPS"
 L2_FLUSH_BYTES = 256 << 20
-CUBLAS_REPS = 5      # torch.mm context launches per size (not the library)
 
 
 def _dist():
@@ -262,29 +262,35 @@ def run_gpu(args):
                        for n in SIZES}
 
     # ---- context only (not on the library's path): cuBLAS through torch.mm on the same operands,
-    # timed with the same flush, device-side wait and events, a few launches per size
+    # with the offline protocol above (per size W warm-up launches, then K launches back to back,
+    # each after the same flush and device-side wait, CUDA events), so the two arms meet the same
+    # power state; the library's offline per-size medians are the figures to compare with
     context = None
     if not args.no_cublas:
         ctx = {}
         for n in SIZES:
             A, B, C = ops[n]
-            for _ in range(2):
+            for _ in range(args.warmup):
+                flush.fill_(1.0)
                 torch.mm(A, B.t(), out=C)
-            ts = []
-            for _ in range(CUBLAS_REPS):
+            torch.cuda.synchronize(dev)
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(args.steps)]
+            for e0, e1 in pairs:
                 flush.fill_(1.0)
                 torch.cuda._sleep(HOST_COVER_CYCLES)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 torch.mm(A, B.t(), out=C)
                 e1.record(stream)
-                torch.cuda.synchronize(dev)
-                ts.append(e0.elapsed_time(e1))
-            med = statistics.median(ts)
+            torch.cuda.synchronize(dev)
+            med = statistics.median(e0.elapsed_time(e1) for e0, e1 in pairs)
             ctx[str(n)] = {"median_ms": round(med, 4), "tflops": round(2.0 * n ** 3 / (med * 1e-3) / 1e12, 1)}
-        context = {"torch_mm_cublas": ctx, "reps": CUBLAS_REPS,
-                   "note": "context line, not the library: torch.mm (cuBLAS) on the same BF16 operands, "
-                           "single launches after the same L2 flush and device-side wait, CUDA events"}
+        flops = sum(2.0 * n ** 3 for n in SIZES)
+        context = {"torch_mm_cublas": ctx,
+                   "value": round(flops / (sum(ctx[str(n)]["median_ms"] for n in SIZES) * 1e-3) / 1e12, 2),
+                   "note": "context line, not the library: torch.mm (cuBLAS) on the same BF16 operands with the "
+                           "offline protocol (per size W warm-ups, then K launches back to back after the same "
+                           "L2 flush and device-side wait, CUDA events); compare with per_size"}
 
     # ---- roofline of the dominant kernel (largest share of the step)
     peak_burst, peak_sust, hbm, peak_kind = _peaks()
