@@ -486,6 +486,14 @@ def run_case(args):
         h.set_option(lcg.OPT_GROUP_ORDER, args.group_order)
     A, B = synthetic.operands(M, N, K, "normal", 2, "bf16", str(dev))
     C = torch.empty((M, (N + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)[:, :N]
+    if args.torch_mm:
+        # context for captures: cuBLAS (torch.mm) on the same operands, not the library
+        for _ in range(args.reps):
+            torch.mm(A, B.t(), out=C)
+        torch.cuda.synchronize(dev)
+        print(f"case {M}x{N}x{K} torch.mm reps={args.reps}")
+        h.close()
+        return
     for _ in range(args.reps):
         h.run(A, B, C, algo=args.algo)
     torch.cuda.synchronize(dev)
@@ -850,6 +858,7 @@ def main():
     ap.add_argument("--no-cublas", action="store_true", help="skip the torch.mm (cuBLAS) context line")
     ap.add_argument("--case", default=None, help="profiling mode: run one shape 'n' or 'M,N,K' --reps times")
     ap.add_argument("--algo", default="auto", help="algorithm for --case")
+    ap.add_argument("--torch-mm", action="store_true", help="--case: run torch.mm (cuBLAS) instead, for context")
     ap.add_argument("--reps", type=int, default=3, help="launches for --case")
     ap.add_argument("--plain-kernel", type=int, default=0,
                     help="--case/--skinny: 1 single-CTA, 2 CTA-pair, 3 skinny plain kernel")
