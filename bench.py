@@ -728,9 +728,11 @@ def run_race(args):
                     torch.cuda.synchronize()
                     burst[a].append(e0.elapsed_time(e1) * 1e-3)
         out = {"M": M, "N": N, "K": K, "burst_clock": clk.summary()}
+        mma_frac = {"plain": 1.0, "strassen1": 7 / 8, "strassen2": 49 / 64}
         for a in algos:
             t = statistics.median(burst[a])
-            out[a] = {"burst_ms": round(t * 1e3, 3), "burst_tflops": round(flops / t / 1e12, 1)}
+            out[a] = {"burst_ms": round(t * 1e3, 3), "burst_tflops": round(flops / t / 1e12, 1),
+                      "burst_mma_tflops": round(mma_frac.get(a, 1.0) * flops / t / 1e12, 1)}
         for a in algos:
             n = max(3, int(args.race_seconds / max(min(burst[a]), 1e-6)))
             torch.cuda.synchronize()
@@ -745,6 +747,7 @@ def run_race(args):
             cs = clk.summary()
             row = out[a]
             row.update({"sustained_ms": round(t * 1e3, 3), "sustained_tflops": round(flops / t / 1e12, 1),
+                        "sustained_mma_tflops": round(mma_frac.get(a, 1.0) * flops / t / 1e12, 1),
                         "launches": n, "sm_mhz": cs.get("sm_mhz"), "reasons": cs.get("reasons")})
             if cs.get("sm_mhz"):
                 row["tflops_per_mhz"] = round(flops / t / 1e12 / cs["sm_mhz"], 4)
