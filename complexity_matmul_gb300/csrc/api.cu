@@ -312,7 +312,10 @@ int run_skinny(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, in
 
 int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
               int64_t ldb, void* C, int64_t ldc, bool bf16, const Epilogue& ep, cudaStream_t st) {
-  const int variant = plain_variant(h, M, N, K);
+  int variant = plain_variant(h, M, N, K);
+  // a fused epilogue lengthens the wide tiles' epilogue, which does not overlap the next
+  // tile's main loop: 256 x 256 tiles then, unless the caller asked for the wide ones
+  if (variant == 5 && ep.on && h->plain_kernel != 5) variant = 2;
   if (variant == 4) return run_gemv(M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, h->pdl != 0, st);
   if (variant == 3) return run_skinny(h, M, N, K, A, lda, B, ldb, C, ldc, bf16, ep, st);
   PlainLaunch L{};
