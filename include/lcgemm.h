@@ -121,8 +121,8 @@ enum {
                                       the pairs; else single-CTA tiles with split-K), 1 single-CTA
                                       128x256 tiles, 2 CTA-pair (cta_group::2) 256x256 tiles, 3 the
                                       stream-K skinny kernel (M <= 256), 4 the CUDA-core GEMV
-                                      (M <= 4), 5 CTA-pair 256x512 tiles; for 3 and 4 larger M
-                                      choose                                                         */
+                                      (M <= 4), 5 CTA-pair 256x512 tiles (0 takes them for long main
+                                      loops without a fused epilogue); for 3 and 4 larger M choose   */
   LCGEMM_OPT_LCMA_KERNEL = 9,       /* fused one-level Strassen kernel: 0 choose (default), 1
                                       single-CTA 128x128 Groups, 2 CTA-pair 256x256 Groups           */
   LCGEMM_OPT_PDL = 10               /* 1 (default): launch the GEMM kernels (plain tiles, GEMV,
