@@ -183,7 +183,7 @@ double pair_waves(int64_t M, int64_t N, int64_t K, int bn, int pairs, bool split
   const double waves = static_cast<double>(full) + (rem == 0 ? 0.0 : halves ? 0.5 : 1.0);
   double t = waves * (bn / 256);
   if (bn == 512) t += static_cast<double>(full + (rem > 0 ? 1 : 0)) * kWideEpilogueSlabs / kb;
-  if (halves) t += kSplitExchangeSlabs / kb;
+  if (halves) t += kSplitExchangeSlabs * (bn / 256) / kb;
   return t;
 }
 

@@ -96,13 +96,13 @@ constexpr int kTailSplitMinSlabs = 48;
 // (DRAM re-reads of the static order grow with the drift between pairs).
 constexpr int kPairClaimMinWaves = 16;
 // Width of the pair tiles: 256 x 512 tiles (two 256-column MMAs sharing each A
-// slab; a quarter less operand traffic from L2) do ~5 % more work per unit of
-// time than 256 x 256 ones in long main loops (under the power cap ~6 % at
-// 16384^3), but their one accumulator keeps each tile's epilogue out of the next
-// tile's main loop (~3 us, about 10 slabs of a 256 x 256 tile), and a split tail
-// costs an exchange of about as much.  The dispatcher compares the two widths'
-// wave-quantised times with these terms.
-constexpr double kWideTileGain = 1.05;
+// slab; a quarter less operand traffic from L2) do more work per unit of time
+// than 256 x 256 ones in long main loops (~5 % in burst, 3-6 % under the power
+// cap at 8192^3 to 16384^3), but their one accumulator keeps each tile's epilogue
+// out of the next tile's main loop (~3 us, about 10 slabs of a 256 x 256 tile),
+// and a split tail costs an exchange of about as much per 256 columns.  The
+// dispatcher compares the two widths' wave-quantised times with these terms.
+constexpr double kWideTileGain = 1.08;
 constexpr double kWideEpilogueSlabs = 10.0;
 constexpr double kSplitExchangeSlabs = 10.0;
 cudaError_t launch_plain_pair(const PlainLaunch& L, cudaStream_t stream);

@@ -87,14 +87,15 @@ def test_tail_split_from_48_slabs(plan):
 
 def test_pair_tile_width():
     """256 x 512 pair tiles when their wave-quantised time, with ~10 slabs of epilogue per wide tile
-    and less their measured ~5 % per unit of work, beats 256 x 256 tiles: the long main loops of
-    16384^3 (27 waves against 54) and 12288^3 take them; the shapes where they measured slower do
-    not: K = 4096 (1024x14336, 4096x16384: 3-8 % slower), a split wide tail against one narrow
-    wave (1024x4096x14336), 4096^3 and 2048^3.  The model prices whichever the dispatcher takes."""
+    and less the wide tiles' measured 8 % per unit of work, beats 256 x 256 tiles: the long main
+    loops of 16384^3 (27 waves against 54), 12288^3 and 8192^3 take them; the shapes where they
+    measured slower do not: K = 4096 (1024x14336, 4096x16384: 3-8 % slower), a split wide tail
+    against one narrow wave (1024x4096x14336), 4096^3 and 2048^3.  The model prices whichever the
+    dispatcher takes."""
     wide, narrow, auto = (lcg.Handle(lcg.PLANNING_DEVICE) for _ in range(3))
     wide.set_option(lcg.OPT_PLAIN_KERNEL, 5)
     narrow.set_option(lcg.OPT_PLAIN_KERNEL, 2)
-    cases = [((16384, 16384, 16384), wide), ((12288, 12288, 12288), wide),
+    cases = [((16384, 16384, 16384), wide), ((12288, 12288, 12288), wide), ((8192, 8192, 8192), wide),
              ((1024, 14336, 4096), narrow), ((4096, 16384, 4096), narrow), ((1024, 4096, 14336), narrow),
              ((4096, 4096, 4096), narrow), ((2048, 2048, 2048), narrow)]
     for (m, n, k), want in cases:
