@@ -382,7 +382,10 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   if (pair) {
     // C for the tensor stores of whole tiles: 32 x 32 boxes (one epilogue warp's
     // chunk), 64-byte swizzle in shared memory
-    const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    // the map ends at the last whole 16-byte unit of a row (the kernel stores the
+    // remaining < 8 columns from registers: a tensor store writes whole units)
+    const uint64_t cdims[2] = {static_cast<uint64_t>(std::max<int64_t>(N & ~int64_t(7), 8)),
+                               static_cast<uint64_t>(M)};
     const uint64_t cstrides[1] = {static_cast<uint64_t>(ldc) * 2};
     const uint32_t cbox[2] = {32u, 32u};
     if (!encode_map(&L.tmC, bf16, C, 2, cdims, cstrides, cbox, CU_TENSOR_MAP_SWIZZLE_64B)) return LCGEMM_ERR_CUDA;

@@ -223,4 +223,34 @@ __device__ __forceinline__ void store_run(uint16_t* dst, int64_t row, int64_t co
   cast_store<BF16, W>(dst, n, v);
 }
 
+// A tensor store writes whole 16-byte units of a row: a unit that reaches past
+// C's last column is written entire.  The maps of C therefore end at the last
+// whole unit inside C (columns below N rounded down to a multiple of 8), and
+// the rest of a row, fewer than 8 elements, is stored from registers here:
+// v[j0 .. j1) of this lane's run, cast once; dst points at the run's first column.
+template <bool BF16>
+__device__ __forceinline__ void store_cols(uint16_t* dst, const float (&v)[32], int j0, int j1) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j >= j0 && j < j1) dst[j] = static_cast<uint16_t>(pack2(v[j], 0.f, BF16) & 0xffffu);
+}
+
+// Cast of one 32 x 32 chunk of C (lane = row, v = its 32 columns) into a
+// shared-memory box of 32 rows x 64 bytes for a tensor store, laid out in the
+// tensor map's 64-byte swizzle: 16-byte unit j of row r at r * 64 +
+// (j ^ ((r >> 1) & 3)) * 16, so that the warp's stores of one unit hit every
+// bank once per quarter warp.  The caller fences the async proxy before the
+// store reads the box.
+template <bool BF16>
+__device__ __forceinline__ void stage_chunk(uint32_t box, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t addr = box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pack2(v[8 * j], v[8 * j + 1], BF16)),
+                 "r"(pack2(v[8 * j + 2], v[8 * j + 3], BF16)), "r"(pack2(v[8 * j + 4], v[8 * j + 5], BF16)),
+                 "r"(pack2(v[8 * j + 6], v[8 * j + 7], BF16))
+                 : "memory");
+  }
+}
+
 }  // namespace lcg

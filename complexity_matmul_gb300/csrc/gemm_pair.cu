@@ -83,22 +83,6 @@ constexpr int pair_smem_bytes() {
 }
 static_assert(pair_smem_bytes<1>() <= 232448 && pair_smem_bytes<2>() <= 232448, "shared memory budget");
 
-// Cast of one 32 x 32 chunk (lane = row, v = its 32 columns) into a shared-memory
-// box of 32 rows x 64 bytes laid out in the tensor map's 64-byte swizzle: 16-byte
-// unit j of row r at r * 64 + (j ^ ((r >> 1) & 3)) * 16, so that the warp's
-// stores of one unit hit every bank once per quarter warp.
-template <bool BF16>
-__device__ __forceinline__ void stage_chunk(uint32_t box, int lane, const float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t addr = box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pack2(v[8 * j], v[8 * j + 1], BF16)),
-                 "r"(pack2(v[8 * j + 2], v[8 * j + 3], BF16)), "r"(pack2(v[8 * j + 4], v[8 * j + 5], BF16)),
-                 "r"(pack2(v[8 * j + 6], v[8 * j + 7], BF16))
-                 : "memory");
-  }
-}
-
 // Queue of claimed items (DYN).  `item`/`full` are this CTA's; `empty` is the
 // leader CTA's (addressed through the cluster window from either CTA).
 struct ItemQueue {
@@ -165,10 +149,14 @@ __device__ __forceinline__ void emit_chunk(float (&v)[32], int row, int row0, in
   stage_chunk<BF16>(box, lane, v);
   fence_proxy_async_shared();
   __syncwarp();
+  const int n8 = args.N & ~7;   // the map of C ends at the last whole 16-byte unit of a row
   if (lane == 0) {
-    if (row0 < args.M && col < args.N) tma_store_2d(tmC, box, col, row0);
+    if (row0 < args.M && col < n8) tma_store_2d(tmC, box, col, row0);
     bulk_commit();
   }
+  if (col + 32 > n8 && col < args.N && row < args.M)
+    store_cols<BF16>(static_cast<uint16_t*>(args.C) + static_cast<int64_t>(row) * args.ldc + col, v,
+                     max(n8 - col, 0), min(args.N - col, 32));
 }
 
 template <bool BF16, bool EPI, bool DYN, int NB>

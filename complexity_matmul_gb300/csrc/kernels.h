@@ -247,10 +247,19 @@ struct LcmaArgs {
   uint64_t timeout_ns;
   Epilogue ep;                    // applied in C's coordinates when a value is final
   int M, N;                       // C's extents: blocks of zero-padded operands may reach past them
+  int c_tma;                      // CTA-pair path, one level: final values leave through tensor stores
+                                  // of the quadrant maps (else 16-byte stores from registers)
+};
+
+// Tensor maps of C's four quadrant blocks (q = 2 * block row + block column),
+// each clipped to C's extents: boxes of 32 x 32 elements, 64-byte swizzle.
+struct QuadMaps {
+  CUtensorMap q[4];
 };
 
 struct LcmaLaunch {
   CUtensorMap tmA_sum, tmA_raw, tmB_sum, tmB_raw;
+  QuadMaps tmC;
   LcmaArgs args;
   int levels;
   bool bf16;

@@ -32,7 +32,9 @@
 // quadrant is accumulated in FP32 and cast once (numerics paragraphs of the
 // write-up's "从缓存重排到 Cost Model" section).  Each epilogue thread owns one
 // accumulator row and 128 columns; the scratch is laid out column-major per
-// slot so that a warp's 32 rows of one column are one 128-byte line.
+// slot so that a warp's 32 rows of one column are one 128-byte line.  Final
+// quadrant values are cast into 32 x 32 shared-memory boxes (two per warp) and
+// leave through tensor stores of per-quadrant maps of C.
 //
 // Cross-CTA synchronisation (as in the plain CTA-pair kernel):
 //   full[s]   leader's; armed with both CTAs' bytes; both CTAs' copies complete on it
@@ -56,7 +58,10 @@ constexpr int kBBytes = (kTileN / 2) * kBK * 2;  // 16 KB (this CTA's half of B)
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTxBytes = 2 * kStageBytes;
 constexpr int kTmemCols = 2 * kTileN;
-constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr int kCBoxBytes = 32 * 32 * 2;                 // one 32 x 32 chunk of C on its way to a tensor store
+constexpr int kCStageBytes = kEpiWarps * 2 * kCBoxBytes;  // two boxes per epilogue warp
+constexpr int kSmemBytes = kStages * kStageBytes + kCStageBytes + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr int kSlots = 2;
 constexpr int kSlotFloats = kRows * kTileN;      // one slot: 128 rows x 256 columns
 constexpr int kSteps1 = 7;
@@ -330,10 +335,15 @@ __device__ __forceinline__ void apply_outer(const float (&v)[32], int iq, int rl
 // the scratch slots / C according to the step's targets.
 // `col0`: first of this thread's 128 columns inside the tile; `tile_col0`: the
 // tile's first column inside the quadrant; `rloc`: this thread's quadrant row.
+// Final values: with `a.c_tma`, cast into one of the warp's two shared-memory
+// boxes (`sbox`, taken in turn by `nbox`) and written by a tensor store of
+// quadrant map t.quad at (column, `row0q` = the warp's first quadrant row), so
+// that a warp's store moves whole lines instead of one 16-byte piece of 32 rows.
 template <bool BF16>
 __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st, float* scratch, int row,
                                                 const LcmaArgs& a, int rloc, int col0, int tile_col0,
-                                                const float* partner, bool last_step) {
+                                                const float* partner, bool last_step, const QuadMaps* tmC,
+                                                uint32_t sbox, uint32_t& nbox, int row0q) {
   uint16_t* Cp = static_cast<uint16_t*>(a.C);
   const uint64_t pol = l2_policy_evict_last();
 #pragma unroll 1
@@ -393,9 +403,29 @@ __device__ __forceinline__ void consume_product(uint32_t tsrc, const StepOps& st
           const int64_t crow_i = static_cast<int64_t>(qr) * a.mb + rloc;
           uint16_t* crow = Cp + crow_i * a.ldc + static_cast<int64_t>(qc) * a.nb;
           const int64_t gcol = static_cast<int64_t>(qc) * a.nb + qcol;
-          if (rloc < a.mb && qcol < a.nb && crow_i < a.M && gcol < a.N)
-            store_run<BF16, 32>(crow + qcol, crow_i, gcol, min(min(32, a.nb - qcol), static_cast<int>(a.N - gcol)),
-                                v, a.ep);
+          const bool inside = rloc < a.mb && qcol < a.nb && crow_i < a.M && gcol < a.N;
+          const int n = min(min(32, a.nb - qcol), static_cast<int>(a.N - gcol));
+          if (a.c_tma) {
+            if (inside) apply_epilogue<BF16, 32>(crow_i, gcol, n, v, a.ep);
+            const int lane = threadIdx.x & 31;
+            const uint32_t box = sbox + (nbox++ & 1u) * kCBoxBytes;
+            if (lane == 0) bulk_wait_read<1>();   // the store that read this box two chunks ago is done with it
+            __syncwarp();
+            stage_chunk<BF16>(box, lane, v);
+            fence_proxy_async_shared();
+            __syncwarp();
+            // the map clips rows past the quadrant's part of C and ends at its last whole
+            // 16-byte unit of a row; the columns after it are stored from registers
+            const int qcols = min(a.nb, a.N - qc * a.nb), qcols8 = qcols & ~7;
+            if (lane == 0) {
+              if (row0q < min(a.mb, a.M - qr * a.mb) && qcol < qcols8) tma_store_2d(&tmC->q[t.quad], box, qcol, row0q);
+              bulk_commit();
+            }
+            if (qcol + 32 > qcols8 && qcol < qcols && rloc < a.mb && crow_i < a.M)
+              store_cols<BF16>(crow + qcol, v, max(qcols8 - qcol, 0), min(qcols - qcol, 32));
+          } else if (inside) {
+            store_run<BF16, 32>(crow + qcol, crow_i, gcol, n, v, a.ep);
+          }
         }
       }
     }
@@ -406,12 +436,13 @@ template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lcma1_l2_kernel(const __grid_constant__ CUtensorMap tmA_sum, const __grid_constant__ CUtensorMap tmA_raw,
                     const __grid_constant__ CUtensorMap tmB_sum, const __grid_constant__ CUtensorMap tmB_raw,
-                    const LcmaArgs args_in) {
+                    const __grid_constant__ QuadMaps tmC, const LcmaArgs args_in) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sC = sB + kStages * kBBytes;      // 1024-byte aligned: the stages are whole KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + kCStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* pfull = bars + 2 * kStages;
@@ -441,6 +472,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmA_raw);
     prefetch_tensormap(&tmB_sum);
     prefetch_tensormap(&tmB_raw);
+    if (args_in.c_tma)
+      for (int q = 0; q < 4; ++q) prefetch_tensormap(&tmC.q[q]);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -554,6 +587,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int half = ew >> 2;               // which 128 of the 256 columns
     const int row = q * 32 + lane;          // accumulator row inside this CTA's 128
     float* scratch = args_in.scratch + static_cast<int64_t>(blockIdx.x) * kSlots * kSlotFloats;
+    const uint32_t sbox = smem_u32(sC) + ew * 2 * kCBoxBytes;   // this warp's two boxes
+    uint32_t nbox = 0;
     uint32_t buf = 0, buf_phase = 0;
     bool ok = true;
     for (int w = pair; ok && w < args_in.num_items; w += num_pairs) {
@@ -583,7 +618,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tsrc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTileN + half * 128;
         // at the last step of a whole Group, the slots it reads are dead until the next Group
         consume_product<BF16>(tsrc, d_l2_programs[type][s], scratch, row, args_in, rloc, half * 128, nb * kTileN,
-                              partner, s == nsteps - 1 && (type == kItemFull || type == kItemFullMixed));
+                              partner, s == nsteps - 1 && (type == kItemFull || type == kItemFullMixed), &tmC, sbox,
+                              nbox, rloc - lane);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&pempty[buf]), 0));
@@ -597,6 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0 && !args_in.debug_drop) red_release_gpu_add(flag, 1);
       }
     }
+    if (lane == 0) bulk_wait_all();   // the tensor stores have read their boxes and written C
   }
 
   tc_fence_before();
@@ -615,7 +652,7 @@ cudaError_t launch_impl(const LcmaLaunch& L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   return launch_maybe_pdl(kern, L.grid, kThreads, kSmemBytes, st, L.pdl, L.tmA_sum, L.tmA_raw, L.tmB_sum, L.tmB_raw,
-                          L.args);
+                          L.tmC, L.args);
 }
 
 }  // namespace

@@ -216,6 +216,26 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
     a.group_order = h->group_order;
     ll.grid = 2 * std::min(a.num_items, P);
     if (!hier) {
+      // quadrant q of C: rows [qr * mb, qr * mb + mb) and columns [qc * nb, qc * nb + nb),
+      // clipped to C; a map's base must sit on a 16-byte boundary and its row pitch be a
+      // multiple of 16 bytes, else the kernel stores from registers
+      const bool tma_ok = reinterpret_cast<uintptr_t>(C) % 16 == 0 && ldc % 8 == 0 && nb % 8 == 0;
+      a.c_tma = 0;
+      if (tma_ok) {
+        a.c_tma = 1;
+        for (int q = 0; q < 4; ++q) {
+          const int64_t qr = q >> 1, qc = q & 1;
+          const int64_t rows = std::min<int64_t>(mb, Mc - qr * mb), cols = std::min<int64_t>(nb, Nc - qc * nb);
+          // whole 16-byte units only: the kernel stores a row's last < 8 columns itself
+          const uint64_t cdims[2] = {static_cast<uint64_t>(std::max<int64_t>(cols & ~int64_t(7), 8)),
+                                     static_cast<uint64_t>(std::max<int64_t>(rows, 1))};
+          const uint64_t cstrides[1] = {static_cast<uint64_t>(ldc) * 2};
+          const uint32_t cbox[2] = {32u, 32u};
+          const void* base = static_cast<const uint16_t*>(C) + qr * mb * ldc + qc * nb;
+          if (!encode_map(&ll.tmC.q[q], bf16, base, 2, cdims, cstrides, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+            return LCGEMM_ERR_CUDA;
+        }
+      }
       if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
       return LCGEMM_OK;
     }

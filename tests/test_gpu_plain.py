@@ -96,6 +96,26 @@ def test_strided_operands(h):
     assert (Cbig[:, :16] == 7).all() and (Cbig[:, 16 + N:] == 7).all()
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 777, 200), (520, 1001, 136), (64, 5, 72)])
+def test_ragged_n_leaves_neighbours_untouched(h, M, N, K):
+    """C as a column view of a wider matrix, N not a multiple of 8: C matches the oracle bit for bit,
+    with and without a fused epilogue, and no element outside the view is written (a tensor store
+    writes whole 16-byte units of a row, so a row's last partial unit must not go through one)."""
+    A, B = synthetic.operands(M, N, K, "int3", 21, "bf16", "cuda")
+    ldc = (N + 7) // 8 * 8 + 16
+    b = synthetic.matrix(1, N, "int3", 22, "bf16", "cuda")[0]
+    R = padded(M, N, "bf16", synthetic.matrix(M, N, "int3", 23, "bf16", "cuda"))   # 16-byte row starts
+    D64, _ = oracle_epilogue(A, B, "bf16", b, R, "relu")
+    for kw, want in (({}, oracle_c64(A, B, "bf16")), ({"bias": b, "residual": R, "act": "relu"}, D64)):
+        Cbig = torch.full((M, ldc), 7.0, dtype=torch.bfloat16, device="cuda")
+        C = Cbig[:, 8:8 + N]
+        h.run(A, B, C, **kw)
+        torch.cuda.synchronize()
+        assert h.sync_status() == 0
+        assert_bit_exact(C, want, "bf16")
+        assert bool((Cbig[:, :8] == 7).all()) and bool((Cbig[:, 8 + N:] == 7).all())
+
+
 # ---------------------------------------------------------------- square sweep (BF16 N(0,1))
 
 def test_square_2048_full(h):
