@@ -324,6 +324,25 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
   const bool pair = variant == 2 || variant == 5;
   const int bm = pair ? 2 * kPlainBM : kPlainBM;
   L.bn = variant == 5 ? 512 : pair ? 256 : plain_single_bn(M, N, grid_cap(h));
+  L.cluster_k = 1;
+  if (!pair && M <= 32) {
+    // A few rows and a K deep enough for the deep split-K (its chunks summed by a
+    // separate kernel): when 128-column tiles in four K chunks about fill the SMs in
+    // clusters of four, each cluster runs one tile's chunks and sums them in shared
+    // memory instead (N = 4096: 32 tiles on 128 SMs).  With more rows every CTA's
+    // copy of A grows to the size of its slice of B, and the deep split stays ahead
+    // (128 x 4096 x 14336: 38.9 against 36.9 us).
+    const int cap = grid_cap(h);
+    const int64_t num_kb = (K + kPlainBK - 1) / kPlainBK, tiles_bn = (N + L.bn - 1) / L.bn;
+    const int64_t t128 = (N + 127) / 128, cl = t128 * kPlainClusterK;
+    const bool deep_split = tiles_bn < cap / 2 && num_kb >= kSplitKMinSlabs &&
+                            std::min<int64_t>(cap / tiles_bn, num_kb / 16) >= kSeparateReduceSplits;
+    if (deep_split && num_kb >= 16 * kPlainClusterK && cl <= cap && cl * 10 >= int64_t(7) * cap &&
+        t128 <= plain_cluster_capacity()) {
+      L.bn = 128;
+      L.cluster_k = kPlainClusterK;
+    }
+  }
   // one tile row: the A box covers only the rows that exist (a multiple of 8)
   const int a_rows = (!pair && M < kPlainBM) ? static_cast<int>((M + 7) / 8 * 8) : kPlainBM;
   if (!encode_kmajor(&L.tmA, bf16, A, M, K, lda, a_rows)) return LCGEMM_ERR_CUDA;
@@ -355,7 +374,11 @@ int run_plain(lcgemm_ctx* h, int64_t M, int64_t N, int64_t K, const void* A, int
     // never raises the chunk count, so the last arriver sums two or three.
     const int num_kb = a.kb_per_split;
     const int cap = grid_cap(h);
-    if (tiles < cap / 2 && num_kb >= kSplitKMinSlabs) {
+    if (L.cluster_k > 1) {
+      // each cluster: one tile's K chunks, summed in shared memory (no workspace)
+      a.splits = L.cluster_k;
+      a.kb_per_split = (num_kb + L.cluster_k - 1) / L.cluster_k;
+    } else if (tiles < cap / 2 && num_kb >= kSplitKMinSlabs) {
       // chunks of at least 16 slabs: the fix-up's latency grows with the number of chunks
       int splits = std::min<int64_t>(cap / tiles, num_kb / 16);
       splits = std::max(1, std::min(splits, 64));

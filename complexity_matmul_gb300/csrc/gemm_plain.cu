@@ -12,12 +12,19 @@
 // Few tiles and a long K: the launcher cuts each tile's K range into chunks
 // (split-K) on consecutive work items; a chunk's FP32 partial goes to a
 // column-major slot of the workspace, and two or three chunks are summed by
-// the last to arrive, more by splitk_reduce_kernel.  When C has one tile row,
-// every B tile is read once and its loads carry an L2 evict-first policy.
+// the last to arrive, more by splitk_reduce_kernel.  With KC > 1 the KC chunks
+// of a 128-column tile run on the KC CTAs of one cluster instead: each leaves
+// its FP32 partial in its own (drained) operand ring and CTA r sums columns
+// 32r .. 32r + 31 of all KC partials through distributed shared memory, in
+// chunk order, with no workspace, counter or second kernel.  When C has one
+// tile row, every B tile is read once and its loads carry an L2 evict-first
+// policy.
 //
 // Prior art for the tiling, the multi-stage prefetch and the block swizzle:
 // CUDA-L2 summary (gist.science 2512.02551), "discovered techniques" list
 // (double-buffering, multi-step prefetch, block swizzling for L2 hit rate).
+#include <mutex>
+
 #include "kernels.h"
 #include "plain_common.cuh"
 #include "ptx.cuh"
@@ -44,11 +51,18 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-template <int BN, int STAGES, bool BF16, bool EPI>
+// Row pitch (floats) of a cluster-split partial in shared memory: 16-byte rows, and
+// consecutive rows 4 banks apart.
+template <int BN>
+constexpr int kRedPitch = BN + 4;
+
+template <int BN, int STAGES, bool BF16, bool EPI, int KC>
 __global__ void __launch_bounds__(kThreads, 1)
     plain_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const PlainArgs args) {
   using C = Cfg<BN, STAGES>;
+  static_assert(KC == 1 || (BN / KC == 32 && kBM * kRedPitch<BN> * 4 <= STAGES * C::kStageBytes),
+                "a cluster split gives each CTA 32 columns; the partial fits in the ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem;
@@ -93,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
   const int num_kb = (args.K + kBK - 1) / kBK;
   const int num_work = args.num_tiles * args.splits;
+  bool epi_ok = false;   // KC > 1: this epilogue warp's partial is in shared memory
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -193,7 +208,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint16_t* crow = Cp + static_cast<int64_t>(row) * args.ldc;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
-      if (args.splits == 1) {
+      if constexpr (KC > 1) {
+        // one item per CTA: this chunk's FP32 partial into the drained operand ring
+        // (every copy landed and every MMA finished before tfull), row-major
+        float* red = reinterpret_cast<float*>(smem) + (q * 32 + lane) * kRedPitch<BN>;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(red + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        epi_ok = true;
+        break;
+      } else if (args.splits == 1) {
         if constexpr (EPI) {
           // the next chunk's bias / residual loads are in flight while this chunk is finished
           EpiLoads<32> pre;
@@ -267,6 +302,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+  }
+
+  if constexpr (KC > 1) {
+    // every CTA of the cluster has its partial in shared memory (or has given up)
+    cluster_sync();
+    if (warp >= 2 && epi_ok) {
+      const int q = warp & 3;
+      const uint32_t rank = cluster_ctarank();
+      int mb, nb;
+      tile_coords(static_cast<int>(blockIdx.x) / KC, args, mb, nb);
+      const int rloc = q * 32 + lane, row = mb * kBM + rloc;
+      const int col = nb * BN + static_cast<int>(rank) * 32;
+      if (row < args.M && col < args.N) {
+        EpiLoads<32> pre;
+        if constexpr (EPI) load_chunk(row, col, args, pre);
+        const uint32_t mine = smem_u32(smem) + static_cast<uint32_t>((rloc * kRedPitch<BN> + rank * 32) * 4);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll 1
+        for (int s = 0; s < KC; ++s) {   // chunk order
+          const uint32_t src = mapa_shared(mine, static_cast<uint32_t>(s));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = ld_cluster_v4(src + 16 * j);
+            v[4 * j] += x.x;
+            v[4 * j + 1] += x.y;
+            v[4 * j + 2] += x.z;
+            v[4 * j + 3] += x.w;
+          }
+        }
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+        store_chunk<BF16, EPI>(static_cast<uint16_t*>(args.C) + static_cast<int64_t>(row) * args.ldc, row, col, r,
+                               args, &pre);
+      }
+    }
+    // no CTA leaves while the others may still read its shared memory
+    cluster_sync();
   }
 
   tc_fence_before();
@@ -352,15 +427,33 @@ __global__ void __launch_bounds__(kReduceThreads) splitk_reduce_kernel(const Pla
   }
 }
 
-template <int BN, int STAGES, bool BF16, bool EPI>
+template <int BN, int STAGES, bool BF16, bool EPI, int KC = 1>
 cudaError_t launch_impl(const PlainLaunch& L, cudaStream_t stream) {
   using C = Cfg<BN, STAGES>;
-  auto kern = plain_gemm_kernel<BN, STAGES, BF16, EPI>;
+  auto kern = plain_gemm_kernel<BN, STAGES, BF16, EPI, KC>;
   {
     const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     if (e != cudaSuccess) return e;
   }
-  return launch_maybe_pdl(kern, L.grid, kThreads, C::kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
+  if constexpr (KC == 1) {
+    return launch_maybe_pdl(kern, L.grid, kThreads, C::kSmemBytes, stream, L.pdl, L.tmA, L.tmB, L.args);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = KC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.args);
+  }
 }
 
 template <int BN, bool BF16>
@@ -383,6 +476,15 @@ cudaError_t launch_splitk_reduce(const PlainLaunch& L, cudaStream_t stream) {
 }
 
 cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream) {
+  if (L.cluster_k == kPlainClusterK) {
+    if (L.bn != 128 || L.args.splits != kPlainClusterK || L.grid != L.args.num_tiles * kPlainClusterK)
+      return cudaErrorInvalidValue;
+    if (L.args.ep.on)
+      return L.bf16 ? launch_impl<128, 6, true, true, kPlainClusterK>(L, stream)
+                    : launch_impl<128, 6, false, true, kPlainClusterK>(L, stream);
+    return L.bf16 ? launch_impl<128, 6, true, false, kPlainClusterK>(L, stream)
+                  : launch_impl<128, 6, false, false, kPlainClusterK>(L, stream);
+  }
   // the kernel without an epilogue keeps the lean store path
   if (L.args.ep.on) {
     if (L.bn == 256) return L.bf16 ? launch_impl<256, 4, true, true>(L, stream) : launch_impl<256, 4, false, true>(L, stream);
@@ -393,6 +495,40 @@ cudaError_t launch_plain(const PlainLaunch& L, cudaStream_t stream) {
   if (L.bn == 128) return L.bf16 ? launch_impl<128, 6, true, false>(L, stream) : launch_impl<128, 6, false, false>(L, stream);
   if (L.bn == 96) return L.bf16 ? launch_impl<96, 7, true, false>(L, stream) : launch_impl<96, 7, false, false>(L, stream);
   return cudaErrorInvalidValue;
+}
+
+int plain_cluster_capacity() {
+  // per device, once: the occupancy query needs the kernel's shared-memory opt-in
+  static std::mutex mu;
+  static int cached[64];
+  static bool done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cached[dev];
+  using C = Cfg<128, 6>;
+  auto kern = plain_gemm_kernel<128, 6, true, false, kPlainClusterK>;
+  int n = 0;
+  if (set_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kPlainClusterK);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPlainClusterK;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();   // the failed query's error, not a launch's
+    }
+  }
+  cached[dev] = n;
+  done[dev] = true;
+  return n;
 }
 
 }  // namespace lcg

@@ -64,11 +64,19 @@ struct PlainArgs {
   int a_rows;
 };
 
+// Single-CTA plain kernel with the K chunks of a tile on the CTAs of one cluster
+// (summed through distributed shared memory): chunks per tile, 128-column tiles.
+constexpr int kPlainClusterK = 4;
+// Clusters of kPlainClusterK single-CTA plain kernels that fit on the device at once.
+int plain_cluster_capacity();
+
 struct PlainLaunch {
   CUtensorMap tmA, tmB;
   CUtensorMap tmC;      // CTA-pair kernel: C in 32 x 32 boxes, 64-byte swizzle (tensor stores)
   PlainArgs args;
   int bn;               // single-CTA kernel: 96, 128 or 256; CTA-pair kernel: 256 or 512
+  int cluster_k;        // single-CTA kernel: 1, or kPlainClusterK (args.splits chunks of each tile on
+                        // the CTAs of one cluster, grid = tiles x chunks)
   bool bf16;
   int grid;
   bool pdl;             // launch as a programmatic dependent of the kernel before it

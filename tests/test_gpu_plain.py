@@ -116,6 +116,50 @@ def test_ragged_n_leaves_neighbours_untouched(h, M, N, K):
         assert bool((Cbig[:, :8] == 7).all()) and bool((Cbig[:, 8 + N:] == 7).all())
 
 
+# Weight-streaming shapes whose K chunks the single-CTA kernel sums inside clusters of four
+# (M <= 32, N about 4096, deep K), ragged M, N and K included; with the grid capped below the
+# 128 CTAs the same shapes take the split-K path with a separate reduction, and at M = 77 the
+# deep split-K runs regardless.
+CLUSTER_SHAPES = [(16, 4096, 14336, "bf16"), (32, 4096, 14336, "bf16"), (5, 4096, 4096, "f16"),
+                  (23, 4000, 8200, "bf16"), (77, 4000, 8200, "bf16")]
+
+
+@pytest.mark.parametrize("M,N,K,dtype", CLUSTER_SHAPES)
+@pytest.mark.parametrize("max_ctas", [0, 64], ids=["cluster_sum", "capped_grid"])
+def test_k_chunks_summed_in_cluster(M, N, K, dtype, max_ctas):
+    hc = lcg.Handle(0)
+    try:
+        hc.set_option(lcg.OPT_MAX_CTAS, max_ctas)
+        A, B = synthetic.operands(M, N, K, "int3", 31, dtype, "cuda")
+        C = hc.run(A, B, algo="plain")
+        torch.cuda.synchronize()
+        assert hc.sync_status() == 0
+        assert_bit_exact(C, oracle_c64(A, B, dtype), dtype)
+        if M == 16:
+            b = synthetic.matrix(1, N, "int3", 32, dtype, "cuda")[0]
+            R = synthetic.matrix(M, N, "int3", 33, dtype, "cuda")
+            D64, _ = oracle_epilogue(A, B, dtype, b, R, "relu")
+            D = hc.run(A, B, algo="plain", bias=b, residual=R, act="relu")
+            torch.cuda.synchronize()
+            assert hc.sync_status() == 0
+            assert_bit_exact(D, D64, dtype)
+    finally:
+        hc.close()
+
+
+def test_k_chunks_summed_in_cluster_normal():
+    """N(0,1) at the weight-streaming shape: the chunk sums in FP32 stay within the plain tolerance."""
+    hc = lcg.Handle(0)
+    try:
+        A, B = synthetic.operands(16, 4096, 14336, "normal", 34, "bf16", "cuda")
+        C = hc.run(A, B, algo="plain")
+        torch.cuda.synchronize()
+        assert hc.sync_status() == 0
+        assert_close(C, oracle_c64(A, B, "bf16"), "bf16", "plain")
+    finally:
+        hc.close()
+
+
 # ---------------------------------------------------------------- square sweep (BF16 N(0,1))
 
 def test_square_2048_full(h):
