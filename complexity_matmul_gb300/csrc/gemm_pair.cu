@@ -362,24 +362,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (half < 0) {
         // whole tile: each 32 x 32 chunk is finished in registers, cast into one of
         // the warp's two shared-memory boxes and written by a tensor store (full
-        // lines; rows and columns past C are clipped by the tensor map)
+        // lines; rows past C are clipped by the tensor map, a row's last partial
+        // 16-byte unit is stored from registers)
         EpiLoads<32> pre;
-        if constexpr (EPI) load_chunk(row, nb * kBN, args, pre);   // next chunk's bias / residual in flight
+        if constexpr (EPI) {
+          load_chunk(row, nb * kBN, args, pre);   // next chunk's bias / residual in flight
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          const int col = nb * kBN + c * 32;
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
-          EpiLoads<32> cur;
-          if constexpr (EPI) {
-            cur = pre;
+          for (int c = 0; c < kBN / 32; ++c) {
+            const int col = nb * kBN + c * 32;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            const EpiLoads<32> cur = pre;
             if (c + 1 < kBN / 32) load_chunk(row, col + 32, args, pre);
-          }
-          tmem_wait_ld();
-          float v[32];
+            tmem_wait_ld();
+            float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          emit_chunk<BF16, EPI>(v, row, row0, col, sbox + ((nbox++ & 1u) * kCBoxBytes), lane, &tmC, args, &cur);
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            emit_chunk<BF16, EPI>(v, row, row0, col, sbox + ((nbox++ & 1u) * kCBoxBytes), lane, &tmC, args, &cur);
+          }
+        } else {
+          // chunk c + 1's tensor-memory load is in flight while chunk c is cast and
+          // stored (two register sets, the loop unrolled by two)
+          static_assert((kBN / 32) % 2 == 0, "chunks come in pairs");
+          uint32_t ra[32], rb[32];
+          auto finish = [&](const uint32_t (&r)[32], int c) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            emit_chunk<BF16, EPI>(v, row, row0, nb * kBN + c * 32, sbox + ((nbox++ & 1u) * kCBoxBytes), lane, &tmC,
+                                  args, nullptr);
+          };
+          tmem_ld_32x32b_x32(tbase, ra);
+          tmem_wait_ld(ra);
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; c += 2) {
+            tmem_ld_32x32b_x32(tbase + (c + 1) * 32, rb);
+            finish(ra, c);
+            tmem_wait_ld(rb);
+            if (c + 2 < kBN / 32) tmem_ld_32x32b_x32(tbase + (c + 2) * 32, ra);
+            finish(rb, c + 1);
+            tmem_wait_ld(ra);
+          }
         }
       } else {
         // tail tile, K half `half`: the partial of the columns the other half finishes
