@@ -105,3 +105,30 @@ def test_capture_claimed_items():
         assert h.sync_status() == 0
         assert_bit_exact(C, oracle_c64(A, B, "bf16"), "bf16")
     h.close()
+
+
+def test_capture_cluster_k_sums():
+    """The single-CTA kernel whose K chunks are summed inside clusters of four (16 x 4096 x 14336),
+    captured with a fused epilogue and replayed on new operands: a cluster launch inside a graph."""
+    M, N, K = 16, 4096, 14336
+    h = lcg.Handle(0)
+    A, B = synthetic.operands(M, N, K, "int3", 98, "bf16", "cuda")
+    b = synthetic.matrix(1, N, "int3", 99, "bf16", "cuda")[0]
+    R = synthetic.matrix(M, N, "int3", 100, "bf16", "cuda")
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    h.run(A, B, C, algo="plain", bias=b, residual=R, act="relu")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        h.run(A, B, C, algo="plain", bias=b, residual=R, act="relu")
+    for seed in (101, 102):
+        A2, B2 = synthetic.operands(M, N, K, "int3", seed, "bf16", "cuda")
+        A.copy_(A2)
+        B.copy_(B2)
+        C.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert h.sync_status() == 0
+        D64, _ = oracle_epilogue(A, B, "bf16", b, R, "relu")
+        assert_bit_exact(C, D64, "bf16")
+    h.close()
