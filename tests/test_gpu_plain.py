@@ -147,6 +147,34 @@ def test_k_chunks_summed_in_cluster(M, N, K, dtype, max_ctas):
         hc.close()
 
 
+@pytest.mark.parametrize("M,dtype", [(1, "bf16"), (2, "f16")])
+def test_k_chunks_summed_in_cluster_one_or_two_rows(M, dtype):
+    """The single-CTA kernel forced for one or two rows (the default takes the GEMV there): an A box
+    of 8 rows, K chunks summed in clusters of four, with and without a fused epilogue."""
+    hc = lcg.Handle(0)
+    try:
+        hc.set_option(lcg.OPT_PLAIN_KERNEL, 1)
+        N, K = 4096, 4096
+        A, B = synthetic.operands(M, N, K, "int3", 35, dtype, "cuda")
+        C = hc.run(A, B, algo="plain")
+        torch.cuda.synchronize()
+        assert hc.sync_status() == 0
+        assert_bit_exact(C, oracle_c64(A, B, dtype), dtype)
+        b = synthetic.matrix(1, N, "int3", 36, dtype, "cuda")[0]
+        R = synthetic.matrix(M, N, "int3", 37, dtype, "cuda")
+        act = "gelu_tanh" if dtype == "f16" else "relu"
+        D64, pre64 = oracle_epilogue(A, B, dtype, b, R, act)
+        D = hc.run(A, B, algo="plain", bias=b, residual=R, act=act)
+        torch.cuda.synchronize()
+        assert hc.sync_status() == 0
+        if act == "relu":
+            assert_bit_exact(D, D64, dtype)
+        else:
+            assert_epilogue_close(D, D64, pre64, dtype, act)
+    finally:
+        hc.close()
+
+
 def test_k_chunks_summed_in_cluster_normal():
     """N(0,1) at the weight-streaming shape: the chunk sums in FP32 stay within the plain tolerance."""
     hc = lcg.Handle(0)
