@@ -121,7 +121,7 @@ def test_ragged_n_leaves_neighbours_untouched(h, M, N, K):
 # 128 CTAs the same shapes take the split-K path with a separate reduction, and at M = 77 the
 # deep split-K runs regardless.
 CLUSTER_SHAPES = [(16, 4096, 14336, "bf16"), (32, 4096, 14336, "bf16"), (5, 4096, 4096, "f16"),
-                  (23, 4000, 8200, "bf16"), (77, 4000, 8200, "bf16")]
+                  (23, 4000, 8200, "bf16"), (9, 4001, 4104, "bf16"), (77, 4000, 8200, "bf16")]
 
 
 @pytest.mark.parametrize("M,N,K,dtype", CLUSTER_SHAPES)
