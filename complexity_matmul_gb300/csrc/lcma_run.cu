@@ -239,31 +239,34 @@ int run_levels(lcgemm_ctx* h, bool fused, int64_t M, int64_t N, int64_t K, const
       if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
       return LCGEMM_OK;
     }
-    // two levels: outer product po runs the one-level kernel on the inner products
-    // p = 7 * po + pi of the two-level tables; its four inner quadrants go to the
-    // outer targets (stream order, and each launch's wait for the one before it,
-    // keep the outer slots consistent)
-    LcmaOperand as[49], bs[49];
-    for (int p = 0; p < plan.R; ++p) {
-      as[p] = a.a_src[p];
-      bs[p] = a.b_src[p];
-    }
-    a.outer = 1;
-    a.oslot = oslot;
-    a.mbp = static_cast<int>(mbp);
-    a.nbp = static_cast<int>(nbp);
-    for (int step = 0; step < 7; ++step) {
-      const OuterStep& os = kOuterProgram[step];
-      for (int pi = 0; pi < 7; ++pi) {
-        a.a_src[pi] = as[7 * os.product + pi];
-        a.b_src[pi] = bs[7 * os.product + pi];
+    if constexpr (L == 2) {
+      // two levels: outer product po runs the one-level kernel on the inner products
+      // p = 7 * po + pi of the two-level tables; its four inner quadrants go to the
+      // outer targets (stream order, and each launch's wait for the one before it,
+      // keep the outer slots consistent)
+      LcmaOperand as[49], bs[49];
+      for (int p = 0; p < plan.R; ++p) {
+        as[p] = a.a_src[p];
+        bs[p] = a.b_src[p];
       }
-      a.otgt[0] = os.t[0];
-      a.otgt[1] = os.t[1];
-      a.flags = split ? flags + step * grid_cap(h) : nullptr;
-      if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+      a.outer = 1;
+      a.oslot = oslot;
+      a.mbp = static_cast<int>(mbp);
+      a.nbp = static_cast<int>(nbp);
+      for (int step = 0; step < 7; ++step) {
+        const OuterStep& os = kOuterProgram[step];
+        for (int pi = 0; pi < 7; ++pi) {
+          a.a_src[pi] = as[7 * os.product + pi];
+          a.b_src[pi] = bs[7 * os.product + pi];
+        }
+        a.otgt[0] = os.t[0];
+        a.otgt[1] = os.t[1];
+        a.flags = split ? flags + step * grid_cap(h) : nullptr;
+        if (launch_lcma_pair(ll, st) != cudaSuccess) return LCGEMM_ERR_CUDA;
+      }
+      return LCGEMM_OK;
     }
-    return LCGEMM_OK;
+    return LCGEMM_OK;   // (one level: hier is false and the run ended above)
   }
   if (fused) {
     ll.grid = std::min(a.num_groups, grid_cap(h));
