@@ -250,6 +250,27 @@ def test_tail_split_integer_bit_exact(h, M, N, K):
     h.set_option(lcg.OPT_SPLIT, 1)
 
 
+@pytest.mark.parametrize("kernel", [2, 5], ids=["tiles256", "tiles512"])
+def test_tail_split_fp16(kernel):
+    """FP16 through the exchanging tail halves (4352 x 2560 x 6200: 170 tiles of 256 x 256 = 2 waves
+    + 18 split; on 256 x 512 tiles 85 = 1 wave + 9 split), split on and off, bit-exact on integers."""
+    hs = lcg.Handle(0)
+    try:
+        hs.set_option(lcg.OPT_PLAIN_KERNEL, kernel)
+        M, N, K = 4352, 2560, 6200
+        A, B = synthetic.operands(M, N, K, "int3", 27, "f16", "cuda")
+        rows = synthetic.row_sample(M, 256)
+        ref = oracle_c64(A, B, "f16", rows=rows)
+        for split in (1, 0):
+            hs.set_option(lcg.OPT_SPLIT, split)
+            C = hs.run(A, B, algo="plain")
+            torch.cuda.synchronize()
+            assert hs.sync_status() == 0
+            assert_bit_exact(C, ref, "f16", rows=rows)
+    finally:
+        hs.close()
+
+
 # ---------------------------------------------------------------- identities and edge cases
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
